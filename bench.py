@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Bench of the local Muon step one data-parallel rank runs on its shard.
+
+Default workload: one Qwen3-1.7B-shaped layer (q 2048x2048, k/v 1024x2048,
+o 2048x2048, gate/up 6144x2048, down 2048x6144; 50,331,648 elements), fp32
+master/momentum/gradients, bf16 parameter copy, mu=0.95 Nesterov, lr=0.02,
+5 quintic Newton-Schulz steps.  Under torchrun with N ranks the job is N such
+layers partitioned by the alpha-Balanced planner (R=N, alpha=1); each rank steps
+its own shard with no collective inside the step (weak scaling).
+
+Prints ONE JSON line (rank 0).  `value` is milliseconds per shard-step for the
+whole job: the slowest rank's mean step time divided by the number of shards.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Muon step ms per shard; Newton-Schulz TFLOP/s and % of GB300 bf16 peak"
+LR, MU, NS_STEPS = 0.02, 0.95, 5
+BUCKET_CAP = 40_000_000
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def ns_flops(shapes, steps=NS_STEPS):
+    """Dense flops of the three products per Newton-Schulz step: 2m^2n + 2m^3 + 2m^2n."""
+    tot = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        tot += steps * (4 * m * m * n + 2 * m * m * m)
+    return tot
+
+
+def ns_flops_executed(shapes, steps=NS_STEPS, bm=128, bn=256):
+    """Flops the tensor cores execute: 128x256 tiles, symmetric products on upper tiles only."""
+    def cdiv(a, b):
+        return (a + b - 1) // b
+    tot = 0
+    for r, c in shapes:
+        m, n = min(r, c), max(r, c)
+        sym = sum(1 for a in range(cdiv(m, bm)) for b in range(cdiv(m, bn)) if a * bm <= b * bn + bn - 1)
+        kpad_n, kpad_m = cdiv(n, 64) * 64, cdiv(m, 64) * 64
+        gram = sym * 2 * bm * bn * kpad_n
+        poly = sym * 2 * bm * bn * kpad_m
+        upd = cdiv(m, bm) * cdiv(n, bn) * 2 * bm * bn * kpad_m
+        tot += steps * (gram + poly + upd)
+    return tot
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ workloads
+def build_workload(name: str, world: int, rank: int):
+    """Returns (shapes, numels, offsets, buckets, R, alpha, grad_bf16, grad_std, rank_to_run, desc)."""
+    from zero_sharded_gb300 import cz
+    from zero_sharded_gb300 import workloads as wl
+
+    if name == "qwen3-1.7b-layer":
+        w = wl.qwen3_1p7b_layers(world)
+        buckets = cz.cz_make_buckets(w.numels, BUCKET_CAP) if world > 1 else [len(w.numels)]
+        return w, buckets, world, 1.0, rank
+    if name == "tiny":
+        w = wl.tiny()
+        return w, [len(w.numels)], 1, 1.0, 0
+    if name == "qwen3-1.7b-28L":
+        w = wl.qwen3_1p7b_layers(28)
+        return w, [len(w.numels)], 1, 1.0, 0
+    if name == "qwen3-14b-microgroup":
+        w = wl.qwen3_14b_microgroup(64)
+        return w, [len(w.numels)], 1, 1.0, 0
+    if name == "qwen3-32b-shard":
+        # plan the whole 64-layer model, then run the heaviest rank's tensors
+        full = wl.qwen3_32b_reverse()
+        b = cz.cz_make_buckets(full.numels, full.bucket_cap)
+        plan = cz.cz_plan_partition(full.numels, b, full.R, full.alpha)
+        loads = plan.rank_load()
+        heavy = max(range(len(loads)), key=lambda r: loads[r])
+        own = plan.owner()
+        shapes = [s for s, o in zip(full.shapes, own) if o == heavy]
+        w = wl.Workload(f"qwen3-32b-R32-shard{heavy}", shapes, [n for n, o in zip(full.names, own) if o == heavy],
+                        0.02, 1e-3)
+        return w, [len(shapes)], 1, 1.0, 0
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for _, _, flags in rows:
+            for nm, fl in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), flags):
+                if fl.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def time_oracle_sample(shapes, grad_std, seed=0, max_per_shape=1):
+    """Times the fp64 oracle on one tensor of each distinct shape and extrapolates
+    to the whole shard by multiplicity.  Returns (ms_per_step, sample_desc, cores)."""
+    import numpy as np
+
+    from oracle import muon as OM
+
+    distinct = {}
+    for s in shapes:
+        distinct[s] = distinct.get(s, 0) + 1
+    rng = np.random.default_rng(seed)
+    total_ms = 0.0
+    parts = []
+    for (r, c), mult in distinct.items():
+        W = (0.02 * rng.standard_normal((r, c))).astype(np.float32)
+        g = (grad_std * rng.standard_normal((r, c))).astype(np.float32)
+        m = np.zeros((r, c), np.float32)
+        t0 = time.perf_counter()
+        OM.muon_step_tensor(W, g, m, LR, MU, NS_STEPS)
+        dt = (time.perf_counter() - t0) * 1e3
+        total_ms += dt * mult
+        parts.append(f"{r}x{c}")
+    desc = (f"oracle (fp64 NumPy) on one tensor of each distinct shape ({', '.join(parts)}; "
+            f"{len(distinct)} of {len(shapes)} tensors), extrapolated by multiplicity")
+    return total_ms, desc, os.cpu_count() or 1
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from zero_sharded_gb300 import workloads as wl  # noqa: F401  (shapes only)
+
+    w, buckets, R, alpha, _ = build_workload(args.workload, 1, 0)
+    for _ in range(args.warmup):
+        time_oracle_sample(w.shapes, w.grad_std)
+    vals = []
+    desc, cores = "", 1
+    for _ in range(args.steps):
+        ms, desc, cores = time_oracle_sample(w.shapes, w.grad_std)
+        vals.append(ms)
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "matrices": len(w.shapes), "elements": w.total, "ns_steps": NS_STEPS},
+            "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["cz", "reference"], default="cz")
+    ap.add_argument("--workload", default="qwen3-1.7b-layer",
+                    choices=["qwen3-1.7b-layer", "tiny", "qwen3-1.7b-28L", "qwen3-14b-microgroup", "qwen3-32b-shard"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from zero_sharded_gb300 import build as zbuild
+    from zero_sharded_gb300 import cz
+    from zero_sharded_gb300 import workloads as wl
+
+    if not os.path.exists(zbuild.LIB):
+        zbuild.build()
+    w, buckets, R, alpha, my_rank = build_workload(args.workload, world, rank)
+    plan = cz.cz_plan_partition(w.numels, buckets, R, alpha)
+    owner = plan.owner()
+    my_shapes = [s for s, o in zip(w.shapes, owner) if o == my_rank]
+    stream = torch.cuda.Stream(device=dev)
+
+    # synthetic inputs, generated on the device from fixed seeds
+    gdt = torch.bfloat16 if w.grad_bf16 else torch.float32
+    P = wl.draw(w.shapes, w.param_std, 0, device=dev)
+    G = wl.draw(w.shapes, w.grad_std, 1, device=dev, dtype=gdt)
+    M = torch.zeros_like(P)
+    PB = P.to(torch.bfloat16)
+    ws_bytes = cz.cz_workspace_size(plan, my_rank, w.shapes)
+    WS = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB > 129 MB L2
+    sargs = cz.StepArgs(w.offsets, w.shapes)
+    opts = cz.make_opts(param_bf16=PB, workspace=WS, workspace_bytes=ws_bytes, grad_is_bf16=w.grad_bf16)
+
+    def step():
+        cz.cz_muon_step_ex(plan, my_rank, P, G, M, sargs, LR, MU, NS_STEPS, stream, opts)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    st = cz.cz_device_status(stream, WS)
+    if st != cz.CZ_OK:
+        raise SystemExit(f"device status after warm-up: {cz.cz_status_string(st)}")
+
+    # ---------------- timed region: K steps, L2 flushed between steps (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    st = cz.cz_device_status(stream, WS)
+    if st != cz.CZ_OK:
+        raise SystemExit(f"device status after timed steps: {cz.cz_status_string(st)}")
+    my_ms = statistics.mean(step_ms)
+    t = torch.tensor([my_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+
+    # ---------------- per-kernel times (library event tracing), same steps again
+    cz.cz_profile_enable(True)
+    cz.cz_profile_read()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            step()
+    torch.cuda.synchronize()
+    prof = cz.cz_profile_read()
+    cz.cz_profile_enable(False)
+    launches_per_step = sum(c for _, c in prof.values()) / args.steps
+    ns_kinds = ("ns_gram", "ns_poly", "ns_update", "ns_update_apply")
+    ns_ms = sum(prof[k][0] for k in ns_kinds) / args.steps
+    ns_launch = sum(prof[k][1] for k in ns_kinds) / args.steps
+    mom_ms = prof["momentum"][0] / args.steps
+
+    peaks, peak_src = load_peaks()
+    F = ns_flops(my_shapes)
+    F_exec = ns_flops_executed(my_shapes)
+    ns_tflops = F / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0
+    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    el = sum(r * c for r, c in my_shapes)
+    mom_bytes = el * (12 + (2 if w.grad_bf16 else 4))          # read g, m; write m, bf16 X
+    mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9 if mom_ms > 0 else 0.0
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+
+    # ---------------- end to end: host gradients in, bf16 parameters out, every step
+    e2e = None
+    if not args.no_e2e:
+        Gh = G.to("cpu").pin_memory()
+        PBh = torch.empty(PB.shape, dtype=PB.dtype).pin_memory()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush.zero_()
+                j = i - args.warmup
+                if j >= 0:
+                    es[j].record(stream)
+                G.copy_(Gh, non_blocking=True)
+                step()
+                PBh.copy_(PB, non_blocking=True)
+                if j >= 0:
+                    ee[j].record(stream)
+        torch.cuda.synchronize()
+        e_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(es, ee))
+        te = torch.tensor([e_ms], device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": float(te.item()) / world, "unit": "ms",
+               "h2d_bytes_per_step": int(G.numel() * G.element_size()),
+               "d2h_bytes_per_step": int(PB.numel() * PB.element_size())}
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cms, desc, cores = time_oracle_sample(my_shapes, w.grad_std)
+            cpu = {"value": cms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": desc}
+        line = {
+            "metric": METRIC, "value": max_ms / world, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "matrices": len(my_shapes), "elements": el, "ns_steps": NS_STEPS,
+                       "R": R, "alpha": alpha, "l2": "flushed: 256 MiB write between timed steps",
+                       "grad": "bf16" if w.grad_bf16 else "fp32", "parallelism": f"dp{world}"},
+            "roofline": {"bound": "tensor", "kernel": "ns_gemm (Gram, Poly, Update, Update+apply)",
+                         "achieved": ns_tflops, "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": ns_tflops / peak_t if peak_t else None, "traffic": None,
+                         "peak_source": f"bf16_tflops_sustained of {peak_src}",
+                         "flops_per_step": F, "executed_flops_per_step": F_exec,
+                         "executed_tflops": F_exec / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else None,
+                         "launches_per_step": ns_launch, "ms_per_step": ns_ms},
+            "momentum_pass": {"bound": "hbm", "achieved": mom_gbs, "peak": hbm, "unit": "GB/s",
+                              "frac": mom_gbs / hbm if hbm else None, "bytes_per_element": mom_bytes / max(el, 1),
+                              "ms_per_step": mom_ms, "peak_source": f"hbm_gbs of {peak_src}"},
+            "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clk, "wall_s_timed_region": wall,
+            "planner": plan.metrics(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,174 @@
+/*
+ * cz.h -- C-ABI of libcz: the alpha-Balanced ZeRO-1 partition planner and the
+ * local Muon step that one data-parallel rank runs on the whole tensors it owns.
+ *
+ * Source of the operations: "Canzona: A Unified, Asynchronous, and Load-Balanced
+ * Framework for Distributed Matrix-based Optimizers" (arXiv 2602.06079), as
+ * summarised on the paper-graph-ui page, section 3.4:
+ *   - "Paradigm 3: Static Partitioning", Eq. 1 (start-index ownership rule);
+ *   - "The DP Load-Balance Optimization Problem" (J_DP, J_Comm, Phi_i(u));
+ *   - "The alpha-Balanced Greedy LPT Algorithm (Algorithm 1)";
+ *   - "Runtime Static-Layout Enforcement": the optimizer step runs on each rank's
+ *     intervals [s_{i,r-1}, s_{i,r}) with zero communication.
+ * The Muon step itself (momentum, Frobenius normalisation, Newton-Schulz,
+ * shape scale, apply) is the standard Muon update; the pages only name it
+ * (section 2: Muon orthogonalises weight matrices with Newton-Schulz iterations;
+ * section 4.1: Delta W = Muon_step(G, States_local)).
+ *
+ * Conventions for every call:
+ *   - Every function returns a status: CZ_OK (0) or a negative CZ_ERR_* code.
+ *     No call aborts, traps or prints.  Invalid arguments are rejected on the
+ *     host before any GPU work is enqueued.
+ *   - Ranks are 0-based.  Sizes are element counts (int64).
+ *   - Host arrays (numels, offsets, shapes, ...) are read during the call only;
+ *     the library keeps no pointer to them.
+ *   - Device buffers are owned by the caller.  The library owns only cz_plan
+ *     objects (host heap) and, when the caller passes no workspace, one cached
+ *     device workspace per device (see cz_muon_step).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     GPU calls are asynchronous on it; CZ_OK means "enqueued".
+ */
+#ifndef CZ_H
+#define CZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CZ_OK                  0
+#define CZ_ERR_INVALID        -1  /* bad argument (sizes, ranks, alpha, shapes, ...)   */
+#define CZ_ERR_CUDA           -2  /* a CUDA runtime/driver call failed                 */
+#define CZ_ERR_NOMEM          -3  /* workspace too small or allocation failed          */
+#define CZ_ERR_PLAN_MISMATCH  -4  /* offsets/shapes do not describe the planned tensors */
+#define CZ_ERR_TIMEOUT        -5  /* a device-side wait ran out (reported by status)   */
+#define CZ_ERR_DEVICE_CHECK   -6  /* a device-side bounds/descriptor check failed      */
+#define CZ_ERR_UNSUPPORTED    -7  /* no sm_103a device, or a feature not built         */
+
+typedef struct cz_plan cz_plan;   /* opaque, immutable after creation, thread-safe to share */
+
+/* Bucket formation (section 3.4, "Problem setup": buckets are ordered,
+ * non-splittable parameter sequences).  Walks numels[0..n_params) in buffer
+ * order and closes a bucket as soon as its element count is >= cap_elems; a
+ * trailing partial bucket is kept.  counts_out must hold n_params entries;
+ * *n_buckets_out receives the number written. */
+int cz_make_buckets(const int64_t* numels, int64_t n_params, int64_t cap_elems,
+                    int64_t* counts_out, int64_t* n_buckets_out);
+
+/* Algorithm 1, alpha-Balanced Greedy LPT, cost W(p) = numel(p).
+ * numels: n_params positive element counts in buffer order.
+ * bucket_sizes: n_buckets positive parameter counts, consecutive, summing to n_params.
+ * R >= 1 ranks, alpha in [0, 1].  Buckets are processed in LPT order (W desc,
+ * index asc); per bucket, deficits d_r = max(0, mu - L_r), target
+ * v* = (1-alpha)/R + alpha d_r/D (1/R when D = 0), cumulative target C, and the
+ * cut s_{k,r} = argmin_{u in [s_{k,r-1}, n_k]} |Phi_k(u) - C| (ties: smaller u);
+ * the last rank takes the remainder.  IEEE double, no contraction: bit-exact
+ * with the reference planner.  *out receives a new plan (free with cz_plan_free). */
+int cz_plan_partition(const int64_t* numels, int64_t n_params,
+                      const int64_t* bucket_sizes, int64_t n_buckets,
+                      int32_t R, double alpha, cz_plan** out);
+
+/* Eq. 1, the start-index split: parameter p at element offset o inside bucket
+ * B_i goes to rank floor(o * R / |B_i|), i.e. r*S <= o < (r+1)*S, S = |B_i|/R. */
+int cz_plan_naive(const int64_t* numels, int64_t n_params,
+                  const int64_t* bucket_sizes, int64_t n_buckets,
+                  int32_t R, cz_plan** out);
+
+void cz_plan_free(cz_plan* plan);   /* NULL is accepted */
+
+/* Sizes of a plan, so that callers can size the query buffers below. */
+int cz_plan_info(const cz_plan* plan, int64_t* n_params, int64_t* n_buckets, int32_t* R);
+
+/* owner_out[n_params]: the 0-based rank that owns each parameter. */
+int cz_plan_owner(const cz_plan* plan, int32_t* owner_out);
+
+/* Slicing vectors s_i in physical bucket order, n_buckets*(R+1) entries each:
+ * param_cuts in parameter indices within the bucket, elem_cuts = Phi_i(s_{i,r})
+ * (element offsets within the bucket).  Either pointer may be NULL. */
+int cz_plan_cuts(const cz_plan* plan, int64_t* param_cuts, int64_t* elem_cuts);
+
+/* load_out[R]: elements owned by each rank (sum over buckets of L_{i,r}). */
+int cz_plan_rank_load(const cz_plan* plan, int64_t* load_out);
+
+/* R_LB = max_r L_r / mean; J_DP = max_r |L_r - mu| (Eq. 2); J_Comm =
+ * sum_i sum_r |S_{i,r} - |B_i|/R|.  Any pointer may be NULL. */
+int cz_plan_metrics(const cz_plan* plan, double* r_lb, double* j_dp, double* j_comm);
+
+/* Options of the Muon step.  Fill with cz_step_opts_default, then override. */
+typedef struct {
+  int32_t nesterov;        /* 1: u = g + mu*m (default); 0: u = m                       */
+  float   eps;             /* added to ||u||_F (default 1e-7)                           */
+  float   a, b, c;         /* Newton-Schulz coefficients (default 3.4445, -4.7750, 2.0315) */
+  int32_t grad_is_bf16;    /* flat_grad holds bf16 values instead of fp32              */
+  void*   param_bf16;      /* nullable: bf16 copy of the parameters, same flat layout;
+                              written as RNE(new fp32 master) for owned tensors        */
+  void*   workspace;       /* nullable: caller-owned device scratch of workspace_bytes
+                              (>= cz_workspace_size).  NULL: the library's cached one  */
+  size_t  workspace_bytes;
+  float*  debug_update_out;/* nullable: fp32 flat buffer (param layout); receives
+                              lr*sqrt(max(1,rows/cols))*X_K for owned tensors          */
+} cz_step_opts;
+
+void cz_step_opts_default(cz_step_opts* opts);
+
+/* Device scratch needed by cz_muon_step_ex for `rank`'s shard under `plan`
+ * (bf16 Newton-Schulz operands, per-tensor norms, tile lists, status word).
+ * shapes: 2*n_params host int64 (rows, cols per parameter). */
+int cz_workspace_size(const cz_plan* plan, int32_t rank, const int64_t* shapes, size_t* bytes);
+
+/* One Muon step over the tensors that `plan` assigns to `rank`
+ * (section 3.4, "Runtime Static-Layout Enforcement", phase 2).
+ *   flat_param: fp32 master weights, flat_grad: fp32 (or bf16, see opts),
+ *   flat_mom: fp32 momentum -- device buffers in one flat layout; parameter p
+ *   occupies [offsets[p], offsets[p] + rows*cols) row-major (rows x cols = out x in).
+ *   offsets: n_params host int64; shapes: 2*n_params host int64.
+ *   Only tensors with owner == rank are read or written; every other byte of
+ *   every buffer is left untouched.  Per owned tensor (rows x cols):
+ *     m <- mu*m + g;  u = g + mu*m;  X0 = u / (||u||_F + eps), transposed to
+ *     min x max if rows > cols;  ns_steps x { A = X X^T; B = b A + c A A;
+ *     X <- a X + B X };  W <- W - lr*sqrt(max(1, rows/cols)) * X (back in rows x cols).
+ * cz_muon_step uses the defaults of cz_step_opts_default and the library's
+ * cached workspace for the current device (not safe for concurrent calls on
+ * different streams; pass a workspace through cz_muon_step_ex for that).
+ * Requires an sm_103a device.  Errors inside kernels (bounded waits that ran out,
+ * descriptor checks) are reported by cz_device_status. */
+int cz_muon_step(const cz_plan* plan, int32_t rank,
+                 float* flat_param, const void* flat_grad, float* flat_mom,
+                 const int64_t* offsets, const int64_t* shapes,
+                 float lr, float mu, int32_t ns_steps, void* stream);
+
+int cz_muon_step_ex(const cz_plan* plan, int32_t rank,
+                    float* flat_param, const void* flat_grad, float* flat_mom,
+                    const int64_t* offsets, const int64_t* shapes,
+                    float lr, float mu, int32_t ns_steps, void* stream,
+                    const cz_step_opts* opts);
+
+/* Synchronises `stream`, reads and clears the device status word kept in
+ * `workspace` (NULL: the library's cached workspace of the current device).
+ * *status_out = CZ_OK or the first CZ_ERR_* a kernel recorded. */
+int cz_device_status(void* stream, void* workspace, int* status_out);
+
+/* Kernel timing (tracing).  While enabled, every kernel that cz_muon_step(_ex)
+ * launches is bracketed by two CUDA events recorded on the caller's stream;
+ * cz_profile_read synchronises on them and returns, per kernel kind, the summed
+ * milliseconds and launch counts since the previous read (then clears them).
+ * Kinds, in order: 0 momentum pass, 1 norm finalize, 2 Gram (A = X X^T),
+ * 3 Poly (B = bA + cA^2), 4 Update (X <- aX + BX), 5 Update fused with the apply.
+ * ms and launches must hold n_kinds entries (n_kinds <= CZ_KERNEL_KINDS). */
+#define CZ_KERNEL_KINDS 6
+int cz_profile_enable(int32_t on);
+int cz_profile_read(double* ms, int64_t* launches, int32_t n_kinds);
+
+/* Static string for a status code. */
+const char* cz_status_string(int status);
+
+/* Library version and build target, e.g. "cz 0.1 sm_103a". */
+const char* cz_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CZ_H */

@@ -1,0 +1,195 @@
+"""GPU parity of the Muon step (through the C-ABI) against the fp64 CPU oracle.
+
+Bars: momentum within 1e-6 relative; per-tensor update delta within 2e-2 relative
+Frobenius error (bf16 Newton-Schulz vs fp64); the bf16 parameter copy equals RNE
+of the GPU's own fp32 master bit for bit; untouched tensors bit-identical.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import muon as OM
+from zero_sharded_gb300 import cz
+from zero_sharded_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+UPDATE_TOL = 2e-2
+MOM_TOL = 1e-6
+LR, MU = 0.02, 0.95
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+class Run:
+    """One cz_muon_step_ex on the GPU with a debug delta buffer and a bf16 copy."""
+
+    def __init__(self, shapes, R=1, alpha=1.0, buckets=None, seed=0, grad_std=1.0, grad_bf16=False,
+                 param_std=0.02):
+        self.shapes = list(shapes)
+        self.numels = [r * c for r, c in self.shapes]
+        self.offsets = list(np.cumsum([0] + self.numels[:-1]))
+        buckets = buckets or [len(self.shapes)]
+        self.plan = cz.cz_plan_partition(self.numels, buckets, R, alpha)
+        self.owner = self.plan.owner()
+        p = wl.draw(self.shapes, param_std, seed)
+        g = wl.draw(self.shapes, grad_std, seed + 1, dtype=torch.bfloat16 if grad_bf16 else torch.float32)
+        self.grad_bf16 = grad_bf16
+        self.p0 = p.clone()
+        self.g = g.clone()
+        self.m0 = torch.zeros_like(p)
+        dev = torch.device("cuda")
+        self.P = p.to(dev)
+        self.G = g.to(dev)
+        self.M = self.m0.to(dev)
+        self.PB = torch.zeros(p.numel(), dtype=torch.bfloat16, device=dev)
+        self.D = torch.zeros(p.numel(), dtype=torch.float32, device=dev)
+        self.args = cz.StepArgs(self.offsets, self.shapes)
+
+    def step(self, rank=0, ns_steps=5, coeffs=None, nesterov=True):
+        opts = cz.make_opts(param_bf16=self.PB, debug_update_out=self.D, grad_is_bf16=self.grad_bf16,
+                            coeffs=coeffs, nesterov=nesterov)
+        cz.cz_muon_step_ex(self.plan, rank, self.P, self.G, self.M, self.args, LR, MU, ns_steps, None, opts)
+        assert cz.cz_device_status(None, None) == cz.CZ_OK
+        torch.cuda.synchronize()
+
+    def tensor(self, buf, i):
+        r, c = self.shapes[i]
+        o = self.offsets[i]
+        return buf[o:o + r * c].reshape(r, c)
+
+
+def check_against_oracle(run, owned, p_before, m_before, ns_steps=5, coeffs=OM.QUINTIC, tol=UPDATE_TOL,
+                         nesterov=True):
+    P = run.P.cpu()
+    M = run.M.cpu()
+    D = run.D.cpu()
+    PB = run.PB.cpu()
+    g = run.g.float() if run.grad_bf16 else run.g
+    worst = 0.0
+    for i in range(len(run.shapes)):
+        Wg = run.tensor(P, i).numpy()
+        if not owned[i]:
+            assert torch.equal(run.tensor(P, i), run.tensor(p_before, i))
+            assert torch.equal(run.tensor(M, i), run.tensor(m_before, i))
+            continue
+        gi = run.tensor(g, i).numpy()
+        mi = run.tensor(m_before, i).numpy()
+        m_new, u = OM.momentum(gi, mi, MU)
+        if not nesterov:
+            u = m_new.astype(np.float64)
+        X = OM.orthogonalise(u, ns_steps, coeffs)
+        r, c = run.shapes[i]
+        delta = LR * OM.shape_scale(r, c) * X
+        mg = run.tensor(M, i).numpy()
+        assert rel_fro(mg, m_new) <= MOM_TOL, ("momentum", i)
+        dg = run.tensor(D, i).numpy()
+        e = rel_fro(dg, delta)
+        worst = max(worst, e)
+        assert e <= tol, ("update", i, run.shapes[i], e)
+        # the master moved by exactly the delta the kernel reports (fp32 rounding)
+        W0 = run.tensor(p_before, i).numpy().astype(np.float64)
+        assert np.allclose(W0 - dg.astype(np.float64), Wg, rtol=0, atol=2e-7 * max(1.0, np.abs(W0).max()))
+        # bf16 copy = RNE(fp32 master), bit for bit
+        want = OM.bf16_rne(Wg)
+        got = run.tensor(PB, i).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, want), ("bf16 copy", i)
+    return worst
+
+
+def test_tiny_config_single_rank():
+    w = wl.tiny()
+    run = Run(w.shapes, R=1)
+    run.step()
+    check_against_oracle(run, [True] * 6, run.p0, run.m0)
+
+
+def test_tiny_config_two_ranks_partition_and_cross_rank_bit_identity():
+    w = wl.tiny()
+    run = Run(w.shapes, R=2)
+    assert run.owner == [0, 0, 0, 1, 1, 1]
+    run.step(rank=0)
+    after0 = run.P.cpu().clone()
+    check_against_oracle(run, [o == 0 for o in run.owner], run.p0, run.m0)
+    run.step(rank=1)
+    both = run.P.cpu()
+    # the same tensors updated by a single rank owning everything give bit-identical results
+    single = Run(w.shapes, R=1)
+    single.step()
+    assert torch.equal(both, single.P.cpu())
+    assert torch.equal(run.M.cpu(), single.M.cpu())
+    assert not torch.equal(after0, both)
+
+
+@pytest.mark.parametrize("shapes", [
+    [(300, 520), (520, 300), (136, 1000), (1000, 136)],          # several tiles, ragged tails, tall and wide
+    [(129, 257), (257, 129), (7, 9), (1, 33), (33, 1)],           # odd sizes: scalar paths, tiny, vectors
+    [(512, 512), (384, 1280), (1280, 384), (640, 128)],           # exact tiles, mixed groups
+])
+def test_ragged_and_multi_tile_shapes(shapes):
+    run = Run(shapes, R=1, seed=3)
+    run.step()
+    check_against_oracle(run, [True] * len(shapes), run.p0, run.m0)
+
+
+def test_many_same_shape_tensors_and_bf16_grads():
+    shapes = [(256, 768)] * 5 + [(768, 256)] * 4 + [(128, 128)] * 6
+    run = Run(shapes, R=1, seed=5, grad_std=1e-3, grad_bf16=True)
+    run.step()
+    check_against_oracle(run, [True] * len(shapes), run.p0, run.m0)
+
+
+def test_three_steps_teacher_forced():
+    shapes = [(256, 512), (512, 256), (384, 384)]
+    run = Run(shapes, R=1, seed=7, grad_std=1e-3)
+    for step in range(3):
+        p_before = run.P.cpu().clone()
+        m_before = run.M.cpu().clone()
+        if step:
+            g = wl.draw(shapes, 1e-3, 100 + step)
+            run.g = g
+            run.G.copy_(g.cuda())
+        run.step()
+        check_against_oracle(run, [True] * 3, p_before, m_before)
+
+
+def test_single_ns_step_and_other_coefficients():
+    shapes = [(192, 320), (320, 192)]
+    run = Run(shapes, R=1, seed=11)
+    run.step(ns_steps=1)
+    check_against_oracle(run, [True, True], run.p0, run.m0, ns_steps=1)
+    # the cubic Newton-Schulz iteration through the same kernels
+    run2 = Run(shapes, R=1, seed=11)
+    run2.step(ns_steps=8, coeffs=OM.CUBIC)
+    check_against_oracle(run2, [True, True], run2.p0, run2.m0, ns_steps=8, coeffs=OM.CUBIC)
+
+
+def test_plain_momentum_without_nesterov():
+    shapes = [(256, 256), (128, 384)]
+    run = Run(shapes, R=1, seed=13)
+    run.step(nesterov=False)
+    check_against_oracle(run, [True, True], run.p0, run.m0, nesterov=False)
+
+
+def test_qwen3_1p7b_layer_full_size():
+    """The bench workload at full size: every tensor checked against the fp64 oracle."""
+    w = wl.qwen3_1p7b_layers(1)
+    run = Run(w.shapes, R=1, seed=0, grad_std=w.grad_std)
+    run.step()
+    worst = check_against_oracle(run, [True] * len(w.shapes), run.p0, run.m0)
+    assert worst < UPDATE_TOL
+
+
+def test_deterministic_repeat():
+    shapes = [(384, 1024), (1024, 384), (256, 256)]
+    a = Run(shapes, R=1, seed=17)
+    b = Run(shapes, R=1, seed=17)
+    a.step()
+    b.step()
+    assert torch.equal(a.P.cpu(), b.P.cpu())
+    assert torch.equal(a.D.cpu(), b.D.cpu())

@@ -1,0 +1,137 @@
+"""C-ABI planner (libcz) against the planner oracle, bit for bit, plus ABI surface checks.
+
+No GPU needed: the planner is host code and the library loads without a device.
+"""
+
+import math
+import os
+import random
+import re
+
+import pytest
+
+from oracle import planner as O
+from zero_sharded_gb300 import cz
+from zero_sharded_gb300 import workloads as wl
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "cz.h")
+
+
+def _same_plan(c_plan, o_plan):
+    pc, ec = c_plan.cuts()
+    assert pc == o_plan.param_cuts
+    assert ec == o_plan.elem_cuts
+    assert c_plan.owner() == o_plan.owner
+    assert c_plan.rank_load() == o_plan.rank_load
+    cm, om = c_plan.metrics(), O.metrics(o_plan)
+    for k in ("r_lb", "j_dp", "j_comm"):
+        assert cm[k] == om[k], k          # bit-exact doubles
+
+
+def test_header_symbols_exported():
+    text = open(HEADER).read()
+    names = sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|void)\s+(cz_\w+)\s*\(", text, re.M)))
+    assert len(names) >= 15
+    lib = cz.load()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert cz.cz_version().endswith("sm_103a")
+
+
+def test_tiny_config_bit_exact():
+    w = wl.tiny()
+    for buckets in ([6], [1] * 6, [2, 4], [3, 3]):
+        for alpha in (0.0, 0.25, 0.5, 1.0):
+            _same_plan(cz.cz_plan_partition(w.numels, buckets, 2, alpha), O.plan_partition(w.numels, buckets, 2, alpha))
+        _same_plan(cz.cz_plan_naive(w.numels, buckets, 2), O.plan_naive(w.numels, buckets, 2))
+
+
+def test_qwen3_32b_layout_bit_exact():
+    w = wl.qwen3_32b_reverse()
+    b_c = cz.cz_make_buckets(w.numels, w.bucket_cap)
+    b_o = O.make_buckets(w.numels, w.bucket_cap)
+    assert b_c == b_o and len(b_c) == 320
+    for R, alpha in ((32, 1.0), (32, 0.5), (16, 1.0), (128, 1.0), (32, 0.0)):
+        _same_plan(cz.cz_plan_partition(w.numels, b_c, R, alpha), O.plan_partition(w.numels, b_o, R, alpha))
+    _same_plan(cz.cz_plan_naive(w.numels, b_c, 32), O.plan_naive(w.numels, b_o, 32))
+
+
+def test_random_layouts_bit_exact():
+    rng = random.Random(1234)
+    for it in range(2000):
+        n = rng.randint(1, 40)
+        numels = [rng.choice([rng.randint(1, 50), rng.randint(1, 5000), rng.randint(1, 10 ** 7)]) for _ in range(n)]
+        cap = rng.randint(1, max(1, sum(numels)))
+        buckets = O.make_buckets(numels, cap)
+        assert cz.cz_make_buckets(numels, cap) == buckets
+        R = rng.choice([1, 2, 3, 5, 8, 13, 32])
+        alpha = rng.choice([0.0, 1.0, rng.random()])
+        _same_plan(cz.cz_plan_partition(numels, buckets, R, alpha), O.plan_partition(numels, buckets, R, alpha))
+        if it % 4 == 0:
+            _same_plan(cz.cz_plan_naive(numels, buckets, R), O.plan_naive(numels, buckets, R))
+
+
+def test_goldens_through_the_abi():
+    import json
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "planner_alpha_blend.json")))
+    for case in g["cases"]:
+        p = cz.cz_plan_partition(g["numels"], g["bucket_sizes"], g["R"], case["alpha"])
+        assert p.cuts()[0] == case["param_cuts"]
+        assert p.rank_load() == case["rank_load"]
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "eq1_start_index_example.json")))
+    assert cz.cz_plan_naive(g["numels"], g["bucket_sizes"], g["R"]).owner() == g["owner"]
+
+
+def test_host_validation_returns_errors():
+    lib = cz.load()
+    with pytest.raises(cz.CzError) as e:
+        cz.cz_plan_partition([1, 2], [2], 0, 1.0)
+    assert e.value.status == cz.CZ_ERR_INVALID
+    for bad in (([1, 2], [2], 2, -0.1), ([1, 2], [2], 2, 1.01), ([1, 2], [1], 2, 1.0), ([1, -2], [2], 2, 1.0),
+                ([1, 2], [3], 2, 1.0), ([1, 2], [1, 0, 1], 2, 1.0)):
+        with pytest.raises(cz.CzError):
+            cz.cz_plan_partition(*bad)
+    with pytest.raises(cz.CzError):
+        cz.cz_plan_partition([1, 2], [2], 2, math.nan)
+    with pytest.raises(cz.CzError):
+        cz.cz_make_buckets([1, 2], 0)
+    assert lib.cz_plan_info(None, None, None, None) == cz.CZ_ERR_INVALID
+    lib.cz_plan_free(None)
+
+
+def test_step_validation_before_any_gpu_work():
+    """Invalid step arguments are rejected on the host (no device is touched)."""
+    w = wl.tiny()
+    p = cz.cz_plan_partition(w.numels, [6], 2, 1.0)
+    args = cz.StepArgs(w.offsets, w.shapes)
+    fake = 0x1000
+    for rank in (-1, 2):
+        with pytest.raises(cz.CzError) as e:
+            cz.cz_muon_step(p, rank, fake, fake, fake, args, 0.02, 0.95, 5)
+        assert e.value.status == cz.CZ_ERR_INVALID
+    with pytest.raises(cz.CzError) as e:
+        cz.cz_muon_step(p, 0, fake, fake, fake, args, 0.02, 0.95, 0)
+    assert e.value.status == cz.CZ_ERR_INVALID
+    bad_shapes = cz.StepArgs(w.offsets, [(64, 64)] * 6)
+    with pytest.raises(cz.CzError) as e:
+        cz.cz_muon_step(p, 0, fake, fake, fake, bad_shapes, 0.02, 0.95, 5)
+    assert e.value.status == cz.CZ_ERR_PLAN_MISMATCH
+    overlap = cz.StepArgs([0] * 6, w.shapes)
+    with pytest.raises(cz.CzError) as e:
+        cz.cz_muon_step(p, 0, fake, fake, fake, overlap, 0.02, 0.95, 5)
+    assert e.value.status == cz.CZ_ERR_PLAN_MISMATCH
+    with pytest.raises(cz.CzError) as e:
+        cz.cz_muon_step(p, 0, None, fake, fake, args, 0.02, 0.95, 5)
+    assert e.value.status == cz.CZ_ERR_INVALID
+
+
+def test_workspace_size_grows_with_shard():
+    w = wl.qwen3_1p7b_layers(1)
+    p1 = cz.cz_plan_partition(w.numels, [len(w.numels)], 1, 1.0)
+    p2 = cz.cz_plan_partition(w.numels, [len(w.numels)], 2, 1.0)
+    s1 = cz.cz_workspace_size(p1, 0, w.shapes)
+    s2 = sum(cz.cz_workspace_size(p2, r, w.shapes) for r in range(2))
+    # bf16 X, two X^T, A and B per tensor dominate: ~6 mn + 4 m^2 bytes
+    approx = sum(6 * r * c + 4 * min(r, c) ** 2 for r, c in w.shapes)
+    assert approx <= s1 <= approx * 1.05
+    assert s2 >= s1 * 0.95

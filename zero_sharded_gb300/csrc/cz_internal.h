@@ -1,0 +1,31 @@
+// Internal declarations shared by the host planner, the step orchestration and
+// the CUDA kernels of libcz.  Not part of the C-ABI (see include/cz.h).
+#pragma once
+
+#include <stdint.h>
+
+#include <vector>
+
+#include "cz.h"
+
+struct cz_plan {};   // the opaque handle type of the C-ABI; cz::Plan derives from it
+
+namespace cz {
+
+struct Plan : cz_plan {
+  int32_t R = 1;
+  int64_t n_params = 0, n_buckets = 0;
+  int kind = 0;              // 0: Algorithm 1, 1: Eq. 1 start-index split
+  double alpha = 0.0;
+  std::vector<int64_t> numels, bucket_sizes;
+  std::vector<int64_t> bucket_first;   // first parameter of each bucket (+ end)
+  std::vector<int64_t> phi_first;      // start of each bucket's Phi in `phi` (+ end)
+  std::vector<int64_t> phi;            // Phi_i(u), u = 0..n_i, concatenated
+  std::vector<int64_t> param_cuts;     // n_buckets*(R+1)
+  std::vector<int64_t> elem_cuts;      // n_buckets*(R+1)
+  std::vector<int32_t> owner;          // n_params
+  std::vector<int64_t> rank_load;      // R
+  double r_lb = 0, j_dp = 0, j_comm = 0;
+};
+
+}  // namespace cz

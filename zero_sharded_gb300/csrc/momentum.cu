@@ -1,0 +1,174 @@
+// Momentum pass of the Muon step: one streaming kernel over the owned tensors.
+//
+// Per element:  m <- mu*m + g  (fp32, stored);  u = g + mu*m  (Nesterov) or u = m;
+// u is written as bf16 twice, in the tensor's rows x cols orientation and
+// transposed, because the Newton-Schulz GEMMs read X (min x max) and X^T with
+// both operands K-major; and sum(u^2) is reduced per tensor for the Frobenius
+// normalisation, deterministically (fixed shuffle tree, fixed block order, then
+// a fixed-order per-tensor sum in double), so results do not depend on timing.
+//
+// HBM traffic per element: read g (4 or 2 B) and m (4 B), write m (4 B) and two
+// bf16 copies (2 + 2 B).
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "step_kernels.h"
+
+namespace cz {
+
+namespace {
+
+constexpr int kTile = 64;
+constexpr int kThreads = 256;
+constexpr int kTrPitch = 65;   // odd pitch: the transposed smem writes are bank-conflict free
+
+__device__ __forceinline__ void load_grad4(const void* grad, int64_t idx, bool bf16, bool vec, int n_ok,
+                                           float* g) {
+  if (bf16) {
+    const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(grad) + idx;
+    if (vec) {
+      uint2 raw = *reinterpret_cast<const uint2*>(gp);
+      __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
+      __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
+      g[0] = __low2float(lo); g[1] = __high2float(lo);
+      g[2] = __low2float(hi); g[3] = __high2float(hi);
+    } else {
+      for (int q = 0; q < 4; ++q) g[q] = q < n_ok ? __bfloat162float(gp[q]) : 0.f;
+    }
+  } else {
+    const float* gp = static_cast<const float*>(grad) + idx;
+    if (vec) {
+      float4 v = __ldcs(reinterpret_cast<const float4*>(gp));
+      g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
+    } else {
+      for (int q = 0; q < 4; ++q) g[q] = q < n_ok ? gp[q] : 0.f;
+    }
+  }
+}
+
+__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(c, d);
+  uint2 r;
+  r.x = *reinterpret_cast<uint32_t*>(&lo);
+  r.y = *reinterpret_cast<uint32_t*>(&hi);
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
+  __shared__ __nv_bfloat16 trT[kTile * kTrPitch];   // trT[c][r]: the tile, transposed
+  __shared__ float warp_sum[kThreads / 32];
+
+  const MomTile t = p.tiles[blockIdx.x];
+  const MomMat mm = p.mats[t.mat];
+  const int tid = threadIdx.x;
+  const bool row_vec = ((mm.off & 3) == 0) && ((mm.cols & 3) == 0);
+  const int cq = (tid & 15) * 4;
+  const int rsub = tid >> 4;
+  const float mu = p.mu;
+  float ss = 0.f;
+
+#pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const int r = rsub + pass * 16;
+    const int gr = t.r0 + r;
+    const int gc = t.c0 + cq;
+    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    if (gr < mm.rows && gc < mm.cols) {
+      const int n_ok = min(4, mm.cols - gc);
+      const int64_t idx = mm.off + (int64_t)gr * mm.cols + gc;
+      const bool vec = row_vec && n_ok == 4;
+      float g[4], m[4];
+      load_grad4(p.grad, idx, p.grad_bf16 != 0, vec, n_ok, g);
+      float* mp = p.mom + idx;
+      if (vec) {
+        float4 v = *reinterpret_cast<const float4*>(mp);
+        m[0] = v.x; m[1] = v.y; m[2] = v.z; m[3] = v.w;
+      } else {
+        for (int q = 0; q < 4; ++q) m[q] = q < n_ok ? mp[q] : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float mn = __fadd_rn(__fmul_rn(mu, m[q]), g[q]);
+        m[q] = mn;
+        u[q] = p.nesterov ? __fadd_rn(g[q], __fmul_rn(mu, mn)) : mn;
+        if (q >= n_ok) u[q] = 0.f;
+      }
+      if (vec) {
+        *reinterpret_cast<float4*>(mp) = make_float4(m[0], m[1], m[2], m[3]);
+      } else {
+        for (int q = 0; q < n_ok; ++q) mp[q] = m[q];
+      }
+      // rows x cols orientation; a partial tail vector lands in the row padding
+      *reinterpret_cast<uint2*>(mm.direct + (int64_t)gr * mm.ld_direct + gc) =
+          pack_bf16x4(u[0], u[1], u[2], u[3]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      ss = fmaf(u[q], u[q], ss);
+      trT[(cq + q) * kTrPitch + r] = __float2bfloat16_rn(u[q]);
+    }
+  }
+  __syncthreads();
+
+  // transposed orientation: rows of u^T are columns of the tile
+#pragma unroll
+  for (int pass = 0; pass < 4; ++pass) {
+    const int c = rsub + pass * 16;
+    const int rq = cq;
+    const int gc = t.c0 + c;
+    const int gr = t.r0 + rq;
+    if (gc < mm.cols && gr < mm.rows) {
+      const __nv_bfloat16* s = trT + c * kTrPitch + rq;
+      __nv_bfloat162 lo = __halves2bfloat162(s[0], s[1]);
+      __nv_bfloat162 hi = __halves2bfloat162(s[2], s[3]);
+      uint2 v;
+      v.x = *reinterpret_cast<uint32_t*>(&lo);
+      v.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(mm.trans + (int64_t)gc * mm.ld_trans + gr) = v;
+    }
+  }
+
+  // deterministic block reduction of sum(u^2)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((tid & 31) == 0) warp_sum[tid >> 5] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) s += warp_sum[w];
+    p.partial[blockIdx.x] = s;
+  }
+}
+
+// One warp per tensor: fixed-order sum of its tiles' partials in double.
+__global__ void __launch_bounds__(128) sigma_finalize_kernel(const MomParams p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= p.n_mats) return;
+  const MomMat mm = p.mats[warp];
+  double s = 0.0;
+  for (int i = lane; i < mm.tile_count; i += 32) s += (double)p.partial[mm.tile_first + i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) p.sigma[warp] = (float)(1.0 / (sqrt(s) + (double)p.eps));
+}
+
+}  // namespace
+
+cudaError_t launch_momentum(const MomParams& p, cudaStream_t s) {
+  if (p.n_tiles <= 0) return cudaSuccess;
+  momentum_kernel<<<p.n_tiles, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sigma_finalize(const MomParams& p, cudaStream_t s) {
+  if (p.n_mats <= 0) return cudaSuccess;
+  const int threads = 128;
+  const int blocks = (p.n_mats * 32 + threads - 1) / threads;
+  sigma_finalize_kernel<<<blocks, threads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace cz

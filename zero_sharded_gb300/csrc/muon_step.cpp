@@ -1,0 +1,707 @@
+// Host orchestration of the local Muon step (cz_muon_step / cz_muon_step_ex).
+//
+// Canzona summary page, section 3.4, "Runtime Static-Layout Enforcement",
+// phase 2: rank r updates exactly the parameters inside its intervals
+// [s_{i,r-1}, s_{i,r}) of every bucket, with no communication, because each
+// owned tensor is whole on the rank.  This file selects the owned tensors from
+// the plan, groups them by Newton-Schulz shape (m = min, n = max of rows/cols),
+// lays out the device workspace, builds TMA tensor maps and LPT-ordered tile
+// lists once per (plan, rank, buffers) and then enqueues, on the caller's stream:
+//   momentum pass -> per-tensor norm -> ns_steps x (Gram, Poly, Update) where
+//   the last Update is the fused apply.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "cz_internal.h"
+#include "step_kernels.h"
+
+namespace cz {
+namespace {
+
+constexpr int64_t kAlign = 256;
+constexpr int64_t kDefaultTimeoutNs = 1000000000LL;   // 1 s per device-side wait
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct OwnedMat {
+  int64_t param;      // parameter index
+  int64_t off;        // element offset
+  int32_t rows, cols;
+  int32_t m, n;       // NS orientation: m = min, n = max
+  bool tall;          // rows > cols: X = u^T
+  int32_t group;
+  int32_t idx;        // index inside the group
+};
+
+struct Group {
+  int32_t m, n, count = 0;
+  int32_t mat_base = 0;        // global matrix index of the group's first matrix
+  int64_t ldx = 0, ldm = 0;    // element pitches: X rows (n), X^T / A / B rows (m)
+  int64_t off_x = 0, off_xt[2] = {0, 0}, off_a = 0, off_b = 0;   // workspace byte offsets
+  bool has_wide = false, has_tall = false;
+};
+
+struct Layout {
+  std::vector<OwnedMat> mats;      // global matrix order (grouped)
+  std::vector<Group> groups;
+  int64_t n_mom_tiles = 0;
+  int64_t off_status = 0, off_sigma = 0, off_partial = 0, off_momtiles = 0, off_mommats = 0, off_matinfo = 0;
+  int64_t off_tiles = 0;           // all GEMM tile lists
+  int64_t n_gemm_tiles = 0;
+  int64_t bytes = 0;
+};
+
+int validate_shapes(const Plan* p, const int64_t* shapes) {
+  for (int64_t i = 0; i < p->n_params; ++i) {
+    const int64_t r = shapes[2 * i], c = shapes[2 * i + 1];
+    if (r <= 0 || c <= 0 || r > (1LL << 30) || c > (1LL << 30)) return CZ_ERR_INVALID;
+    if (r * c != p->numels[i]) return CZ_ERR_PLAN_MISMATCH;
+  }
+  return CZ_OK;
+}
+
+// Owned tensors grouped by (m, n), groups in order of first appearance.
+int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int64_t* shapes, Layout& L) {
+  std::map<std::pair<int32_t, int32_t>, int32_t> gid;
+  std::vector<std::vector<OwnedMat>> per_group;
+  for (int64_t i = 0; i < p->n_params; ++i) {
+    if (p->owner[i] != rank) continue;
+    OwnedMat om;
+    om.param = i;
+    om.off = offsets ? offsets[i] : 0;
+    om.rows = (int32_t)shapes[2 * i];
+    om.cols = (int32_t)shapes[2 * i + 1];
+    om.tall = om.rows > om.cols;
+    om.m = std::min(om.rows, om.cols);
+    om.n = std::max(om.rows, om.cols);
+    auto key = std::make_pair(om.m, om.n);
+    auto it = gid.find(key);
+    if (it == gid.end()) {
+      it = gid.emplace(key, (int32_t)per_group.size()).first;
+      per_group.emplace_back();
+      Group g;
+      g.m = om.m;
+      g.n = om.n;
+      L.groups.push_back(g);
+    }
+    om.group = it->second;
+    per_group[it->second].push_back(om);
+  }
+  int32_t base = 0;
+  for (size_t g = 0; g < per_group.size(); ++g) {
+    Group& G = L.groups[g];
+    G.count = (int32_t)per_group[g].size();
+    G.mat_base = base;
+    for (int32_t j = 0; j < G.count; ++j) {
+      OwnedMat om = per_group[g][j];
+      om.idx = j;
+      G.has_tall |= om.tall;
+      G.has_wide |= !om.tall;
+      L.mats.push_back(om);
+    }
+    base += G.count;
+  }
+  // workspace layout
+  const int64_t n_mats = (int64_t)L.mats.size();
+  for (const OwnedMat& om : L.mats) L.n_mom_tiles += ceil_div64(om.rows, 64) * ceil_div64(om.cols, 64);
+  int64_t off = 0;
+  L.off_status = off;  off += kAlign;
+  L.off_sigma = off;   off = align_up(off + 4 * std::max<int64_t>(n_mats, 1), kAlign);
+  L.off_partial = off; off = align_up(off + 4 * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
+  L.off_momtiles = off; off = align_up(off + (int64_t)sizeof(MomTile) * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
+  L.off_mommats = off; off = align_up(off + (int64_t)sizeof(MomMat) * std::max<int64_t>(n_mats, 1), kAlign);
+  L.off_matinfo = off; off = align_up(off + (int64_t)sizeof(MatInfo) * std::max<int64_t>(n_mats, 1), kAlign);
+  // GEMM tiles: Gram + Poly (same count), and two ping-pong copies each of the
+  // Update and Apply lists (a tall tensor's Apply tiles cover n x m)
+  int64_t nt = 0;
+  for (const Group& G : L.groups) {
+    const int64_t tm = ceil_div64(G.m, kBM), tn = ceil_div64(G.m, kBN);
+    int64_t sym = 0;
+    for (int64_t a = 0; a < tm; ++a)
+      for (int64_t b = 0; b < tn; ++b)
+        if (a * kBM <= b * kBN + kBN - 1) ++sym;
+    const int64_t upd = ceil_div64(G.m, kBM) * ceil_div64(G.n, kBN);
+    const int64_t app_t = ceil_div64(G.n, kBM) * ceil_div64(G.m, kBN);
+    nt += G.count * (2 * sym + 2 * upd + 2 * std::max(upd, app_t));
+  }
+  L.n_gemm_tiles = nt;
+  L.off_tiles = off; off = align_up(off + 16 * std::max<int64_t>(nt, 1), kAlign);
+  for (Group& G : L.groups) {
+    G.ldx = align_up(G.n, 8);
+    G.ldm = align_up(G.m, 8);
+    const int64_t c = G.count;
+    G.off_x = off;     off = align_up(off + 2 * c * G.m * G.ldx, kAlign);
+    G.off_xt[0] = off; off = align_up(off + 2 * c * G.n * G.ldm, kAlign);
+    G.off_xt[1] = off; off = align_up(off + 2 * c * G.n * G.ldm, kAlign);
+    G.off_a = off;     off = align_up(off + 2 * c * G.m * G.ldm, kAlign);
+    G.off_b = off;     off = align_up(off + 2 * c * G.m * G.ldm, kAlign);
+  }
+  L.bytes = off;
+  return CZ_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 3-D bf16 map over `count` matrices of `rows` x `inner` (row pitch ld elements,
+// matrix stride ms elements), box = 64 (inner) x box_rows x 1, 128-byte swizzle.
+bool encode_map(CUtensorMap* map, void* base, int64_t inner, int64_t rows, int64_t count, int64_t ld, int64_t ms,
+                uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)count};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(ms * 2)};
+  cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct Launch {
+  int phase;
+  int first;
+  int cur;                          // X^T ping-pong index read by Update / Apply
+  GemmParams params;
+};
+
+// Everything that depends only on (plan, rank, shapes, offsets, buffers, options).
+struct Program {
+  Layout L;
+  std::vector<uint8_t> host_tables;   // image of [off_sigma .. off_tiles + tiles) region (tables only)
+  int64_t tables_begin = 0, tables_end = 0;
+  MomParams mom{};
+  std::vector<Launch> gram, poly, update[2], apply[2];
+  int grid = 1;
+};
+
+struct Key {
+  const void* plan; int32_t rank; int dev;
+  const void *param, *grad, *mom, *pbf16, *dbg, *ws;
+  int32_t grad_bf16, nesterov, ns_steps;
+  float lr, mu, eps, a, b, c;
+  std::vector<int64_t> offsets, shapes;
+  bool operator<(const Key& o) const {
+    return std::tie(plan, rank, dev, param, grad, mom, pbf16, dbg, ws, grad_bf16, nesterov, ns_steps, lr, mu, eps, a,
+                    b, c, offsets, shapes) < std::tie(o.plan, o.rank, o.dev, o.param, o.grad, o.mom, o.pbf16, o.dbg,
+                                                      o.ws, o.grad_bf16, o.nesterov, o.ns_steps, o.lr, o.mu, o.eps,
+                                                      o.a, o.b, o.c, o.offsets, o.shapes);
+  }
+};
+
+// ---------------------------------------------------------------- tracing
+struct ProfRec { int kind; cudaEvent_t a, b; };
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+
+// Launches `fn` on stream s, bracketed by events when tracing is on.
+template <class F>
+cudaError_t traced(int kind, cudaStream_t s, F&& fn) {
+  if (!g_prof_on) return fn();
+  ProfRec r{kind, nullptr, nullptr};
+  if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return cudaGetLastError();
+  cudaEventRecord(r.a, s);
+  cudaError_t e = fn();
+  cudaEventRecord(r.b, s);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof.push_back(r);
+  return e;
+}
+
+std::mutex g_mu;
+std::map<Key, std::shared_ptr<Program>> g_cache;
+std::map<std::pair<int, const void*>, const Program*> g_resident;   // tables currently uploaded per workspace
+struct DevWs { void* ptr = nullptr; size_t bytes = 0; };
+std::map<int, DevWs> g_ws;
+
+template <class T>
+T* at(std::vector<uint8_t>& img, int64_t base, int64_t off) {
+  return reinterpret_cast<T*>(img.data() + (off - base));
+}
+
+// Tile lists for one phase: {problem, matrix, tile_m, tile_n}, sorted so the
+// longest K goes first (LPT), then chunked into launches of <= kMaxProblems problems.
+struct ProbDesc {
+  GemmProblem gp;
+  CUtensorMap ta, tb;
+  std::vector<int4> tiles;
+};
+
+bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int4* host_tiles, int64_t& tile_cursor,
+                   const GemmParams& common, std::vector<Launch>& out, int first, int cur) {
+  for (size_t c0 = 0; c0 < probs.size(); c0 += kMaxProblems) {
+    const size_t c1 = std::min(probs.size(), c0 + (size_t)kMaxProblems);
+    std::vector<int4> tl;
+    for (size_t i = c0; i < c1; ++i)
+      for (int4 t : probs[i].tiles) tl.push_back(make_int4((int)(i - c0), t.y, t.z, t.w));
+    if (tl.empty()) continue;
+    std::stable_sort(tl.begin(), tl.end(), [&](const int4& x, const int4& y) {
+      return probs[c0 + x.x].gp.K > probs[c0 + y.x].gp.K;
+    });
+    Launch ln;
+    ln.phase = phase;
+    ln.first = first;
+    ln.cur = cur;
+    std::memset(&ln.params, 0, sizeof(GemmParams));
+    ln.params = common;
+    ln.params.n_prob = (int)(c1 - c0);
+    for (size_t i = c0; i < c1; ++i) {
+      ln.params.tmA[i - c0] = probs[i].ta;
+      ln.params.tmB[i - c0] = probs[i].tb;
+      ln.params.prob[i - c0] = probs[i].gp;
+    }
+    ln.params.first = first;
+    ln.params.n_tiles = (int)tl.size();
+    ln.params.tiles = dev_tiles + tile_cursor;
+    std::copy(tl.begin(), tl.end(), host_tiles + tile_cursor);
+    tile_cursor += (int64_t)tl.size();
+    out.push_back(ln);
+  }
+  return true;
+}
+
+int build_program(const Plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
+                  const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps,
+                  const cz_step_opts& o, uint8_t* ws, Program& P) {
+  Layout& L = P.L;
+  int st = build_layout(plan, rank, offsets, shapes, L);
+  if (st != CZ_OK) return st;
+  const int64_t n_mats = (int64_t)L.mats.size();
+  P.tables_begin = L.off_sigma;
+  P.tables_end = L.off_tiles + 16 * L.n_gemm_tiles;
+  P.host_tables.assign((size_t)(P.tables_end - P.tables_begin), 0);
+  auto& img = P.host_tables;
+  const int64_t tb = P.tables_begin;
+
+  // momentum pass tables
+  MomTile* mt = at<MomTile>(img, tb, L.off_momtiles);
+  MomMat* mm = at<MomMat>(img, tb, L.off_mommats);
+  MatInfo* mi = at<MatInfo>(img, tb, L.off_matinfo);
+  int64_t tcur = 0;
+  for (int64_t g = 0; g < n_mats; ++g) {
+    const OwnedMat& om = L.mats[g];
+    const Group& G = L.groups[om.group];
+    uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x) + (int64_t)om.idx * G.m * G.ldx;
+    uint16_t* XT = reinterpret_cast<uint16_t*>(ws + G.off_xt[0]) + (int64_t)om.idx * G.n * G.ldm;
+    MomMat& d = mm[g];
+    d.off = om.off;
+    d.rows = om.rows;
+    d.cols = om.cols;
+    if (!om.tall) {          // X = u (rows x cols), X^T = u^T
+      d.direct = X; d.ld_direct = G.ldx;
+      d.trans = XT; d.ld_trans = G.ldm;
+    } else {                 // X = u^T, X^T = u (rows x cols)
+      d.direct = XT; d.ld_direct = G.ldm;
+      d.trans = X; d.ld_trans = G.ldx;
+    }
+    d.tile_first = (int32_t)tcur;
+    const int64_t tr = ceil_div64(om.rows, 64), tc = ceil_div64(om.cols, 64);
+    d.tile_count = (int32_t)(tr * tc);
+    for (int64_t a = 0; a < tr; ++a)
+      for (int64_t b = 0; b < tc; ++b) {
+        MomTile& t = mt[tcur++];
+        t.mat = (int32_t)g;
+        t.r0 = (int32_t)(a * 64);
+        t.c0 = (int32_t)(b * 64);
+        t.pad = 0;
+      }
+    MatInfo& m = mi[g];
+    m.w_off = om.off;
+    m.rows = om.rows;
+    m.cols = om.cols;
+    m.lrs = (float)((double)lr * std::sqrt(std::max(1.0, (double)om.rows / (double)om.cols)));
+    m.vec_ok = ((om.off & 3) == 0 && (om.cols & 3) == 0) ? 1 : 0;
+  }
+  MomParams& mp = P.mom;
+  mp.mom = flat_mom;
+  mp.grad = flat_grad;
+  mp.grad_bf16 = o.grad_is_bf16 ? 1 : 0;
+  mp.nesterov = o.nesterov ? 1 : 0;
+  mp.mu = mu;
+  mp.eps = o.eps;
+  mp.tiles = reinterpret_cast<const MomTile*>(ws + L.off_momtiles);
+  mp.n_tiles = (int32_t)L.n_mom_tiles;
+  mp.mats = reinterpret_cast<const MomMat*>(ws + L.off_mommats);
+  mp.n_mats = (int32_t)n_mats;
+  mp.partial = reinterpret_cast<float*>(ws + L.off_partial);
+  mp.sigma = reinterpret_cast<float*>(ws + L.off_sigma);
+  mp.status = reinterpret_cast<int*>(ws + L.off_status);
+
+  // GEMM problems
+  GemmParams common;
+  std::memset(&common, 0, sizeof(common));
+  common.sigma = mp.sigma;
+  common.mats = reinterpret_cast<const MatInfo*>(ws + L.off_matinfo);
+  common.a = o.a;
+  common.b = o.b;
+  common.c = o.c;
+  common.W = flat_param;
+  common.Wb = reinterpret_cast<uint16_t*>(o.param_bf16);
+  common.dbg = o.debug_update_out;
+  common.status = mp.status;
+  common.timeout_ns = kDefaultTimeoutNs;
+
+  int4* dev_tiles = reinterpret_cast<int4*>(ws + L.off_tiles);
+  int4* host_tiles = at<int4>(img, tb, L.off_tiles);
+  int64_t cursor = 0;
+  std::vector<ProbDesc> gram, poly, upd[2], app[2];
+  for (const Group& G : L.groups) {
+    uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x);
+    uint16_t* XT[2] = {reinterpret_cast<uint16_t*>(ws + G.off_xt[0]), reinterpret_cast<uint16_t*>(ws + G.off_xt[1])};
+    uint16_t* A = reinterpret_cast<uint16_t*>(ws + G.off_a);
+    uint16_t* B = reinterpret_cast<uint16_t*>(ws + G.off_b);
+    const int64_t msx = (int64_t)G.m * G.ldx, mst = (int64_t)G.n * G.ldm, msa = (int64_t)G.m * G.ldm;
+    const int c = G.count;
+    // symmetric tiles of an m x m output
+    std::vector<int4> sym;
+    for (int j = 0; j < c; ++j)
+      for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
+        for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b)
+          if (a * kBM <= b * kBN + kBN - 1) sym.push_back(make_int4(0, j, (int)a, (int)b));
+    {
+      ProbDesc d;
+      std::memset(&d.gp, 0, sizeof(d.gp));
+      d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.n; d.gp.count = c; d.gp.mat_base = G.mat_base;
+      d.gp.out = A; d.gp.ld_out = G.ldm; d.gp.ms_out = msa;
+      if (!encode_map(&d.ta, X, G.n, G.m, c, G.ldx, msx, kBM) || !encode_map(&d.tb, X, G.n, G.m, c, G.ldx, msx, kBN))
+        return CZ_ERR_CUDA;
+      d.tiles = sym;
+      gram.push_back(d);
+    }
+    {
+      ProbDesc d;
+      std::memset(&d.gp, 0, sizeof(d.gp));
+      d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
+      d.gp.out = B; d.gp.ld_out = G.ldm; d.gp.ms_out = msa;
+      d.gp.aux = A; d.gp.ld_aux = G.ldm; d.gp.ms_aux = msa;
+      if (!encode_map(&d.ta, A, G.m, G.m, c, G.ldm, msa, kBM) || !encode_map(&d.tb, A, G.m, G.m, c, G.ldm, msa, kBN))
+        return CZ_ERR_CUDA;
+      d.tiles = sym;
+      poly.push_back(d);
+    }
+    for (int cur = 0; cur < 2; ++cur) {
+      // update: X (m x n) <- a X + B X; operands B rows (K = m) and X^T rows (K = m)
+      ProbDesc d;
+      std::memset(&d.gp, 0, sizeof(d.gp));
+      d.gp.M = G.m; d.gp.N = G.n; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
+      d.gp.out = X; d.gp.ld_out = G.ldx; d.gp.ms_out = msx;
+      d.gp.out_t = XT[cur ^ 1]; d.gp.ld_out_t = G.ldm; d.gp.ms_out_t = mst;
+      d.gp.aux = X; d.gp.ld_aux = G.ldx; d.gp.ms_aux = msx;
+      if (!encode_map(&d.ta, B, G.m, G.m, c, G.ldm, msa, kBM) ||
+          !encode_map(&d.tb, XT[cur], G.m, G.n, c, G.ldm, mst, kBN))
+        return CZ_ERR_CUDA;
+      for (int j = 0; j < c; ++j)
+        for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
+          for (int64_t b = 0; b < ceil_div64(G.n, kBN); ++b) d.tiles.push_back(make_int4(0, j, (int)a, (int)b));
+      upd[cur].push_back(d);
+      // apply, wide tensors: output X (m x n) = parameter layout
+      if (G.has_wide) {
+        ProbDesc e = d;
+        e.gp.orient = 0;
+        e.gp.out = nullptr; e.gp.out_t = nullptr;
+        e.tiles.clear();
+        for (int j = 0; j < c; ++j) {
+          if (L.mats[G.mat_base + j].tall) continue;
+          for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
+            for (int64_t b = 0; b < ceil_div64(G.n, kBN); ++b) e.tiles.push_back(make_int4(0, j, (int)a, (int)b));
+        }
+        app[cur].push_back(e);
+      }
+      // apply, tall tensors: output X^T (n x m) = parameter layout; operands X^T rows and B rows
+      if (G.has_tall) {
+        ProbDesc e;
+        std::memset(&e.gp, 0, sizeof(e.gp));
+        e.gp.M = G.n; e.gp.N = G.m; e.gp.K = G.m; e.gp.count = c; e.gp.mat_base = G.mat_base;
+        e.gp.orient = 1;
+        e.gp.aux = XT[cur]; e.gp.ld_aux = G.ldm; e.gp.ms_aux = mst;
+        if (!encode_map(&e.ta, XT[cur], G.m, G.n, c, G.ldm, mst, kBM) ||
+            !encode_map(&e.tb, B, G.m, G.m, c, G.ldm, msa, kBN))
+          return CZ_ERR_CUDA;
+        for (int j = 0; j < c; ++j) {
+          if (!L.mats[G.mat_base + j].tall) continue;
+          for (int64_t a = 0; a < ceil_div64(G.n, kBM); ++a)
+            for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b) e.tiles.push_back(make_int4(0, j, (int)a, (int)b));
+        }
+        app[cur].push_back(e);
+      }
+    }
+  }
+  // Gram with first=0/1 share one tile list: build first, copy for the other flag.
+  make_launches(kGram, gram, dev_tiles, host_tiles, cursor, common, P.gram, 0, 0);
+  make_launches(kPoly, poly, dev_tiles, host_tiles, cursor, common, P.poly, 0, 0);
+  for (int cur = 0; cur < 2; ++cur) {
+    make_launches(kUpdate, upd[cur], dev_tiles, host_tiles, cursor, common, P.update[cur], 0, cur);
+    make_launches(kApply, app[cur], dev_tiles, host_tiles, cursor, common, P.apply[cur], 0, cur);
+  }
+  (void)ns_steps;
+  if (cursor > L.n_gemm_tiles) return CZ_ERR_NOMEM;   // cannot happen: sized by build_layout
+  P.grid = gemm_max_grid();
+  return CZ_OK;
+}
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CZ_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return CZ_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return CZ_ERR_CUDA;
+  if (major != 10 || minor != 3) return CZ_ERR_UNSUPPORTED;
+  return CZ_OK;
+}
+
+int get_internal_ws(size_t need, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CZ_ERR_CUDA;
+  DevWs& w = g_ws[dev];
+  if (w.bytes < need) {
+    if (w.ptr) {
+      cudaDeviceSynchronize();
+      cudaFree(w.ptr);
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, need) != cudaSuccess) {
+      cudaGetLastError();
+      return CZ_ERR_NOMEM;
+    }
+    if (cudaMemset(p, 0, kAlign) != cudaSuccess) return CZ_ERR_CUDA;
+    w.ptr = p;
+    w.bytes = need;
+  }
+  *out = w.ptr;
+  return CZ_OK;
+}
+
+}  // namespace
+}  // namespace cz
+
+using namespace cz;
+
+extern "C" {
+
+void cz_step_opts_default(cz_step_opts* o) {
+  if (!o) return;
+  std::memset(o, 0, sizeof(*o));
+  o->nesterov = 1;
+  o->eps = 1e-7f;
+  o->a = 3.4445f;
+  o->b = -4.7750f;
+  o->c = 2.0315f;
+}
+
+int cz_workspace_size(const cz_plan* plan, int32_t rank, const int64_t* shapes, size_t* bytes) {
+  if (!plan || !shapes || !bytes) return CZ_ERR_INVALID;
+  const Plan* p = static_cast<const Plan*>(plan);
+  if (rank < 0 || rank >= p->R) return CZ_ERR_INVALID;
+  int st = validate_shapes(p, shapes);
+  if (st != CZ_OK) return st;
+  Layout L;
+  st = build_layout(p, rank, nullptr, shapes, L);
+  if (st != CZ_OK) return st;
+  *bytes = (size_t)L.bytes;
+  return CZ_OK;
+}
+
+int cz_muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
+                 const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps, void* stream) {
+  cz_step_opts o;
+  cz_step_opts_default(&o);
+  return cz_muon_step_ex(plan, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, stream, &o);
+}
+
+int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
+                    const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps, void* stream,
+                    const cz_step_opts* opts) {
+  if (!plan || !flat_param || !flat_grad || !flat_mom || !offsets || !shapes || !opts) return CZ_ERR_INVALID;
+  const Plan* p = static_cast<const Plan*>(plan);
+  if (rank < 0 || rank >= p->R || ns_steps < 1 || ns_steps > 64) return CZ_ERR_INVALID;
+  if (!std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(opts->eps) || opts->eps < 0.f) return CZ_ERR_INVALID;
+  int st = validate_shapes(p, shapes);
+  if (st != CZ_OK) return st;
+  // parameters must not overlap in the flat layout
+  {
+    std::vector<std::pair<int64_t, int64_t>> iv(p->n_params);
+    for (int64_t i = 0; i < p->n_params; ++i) {
+      if (offsets[i] < 0) return CZ_ERR_INVALID;
+      iv[i] = {offsets[i], offsets[i] + p->numels[i]};
+    }
+    std::sort(iv.begin(), iv.end());
+    for (size_t i = 1; i < iv.size(); ++i)
+      if (iv[i].first < iv[i - 1].second) return CZ_ERR_PLAN_MISMATCH;
+  }
+  bool any = false;
+  for (int64_t i = 0; i < p->n_params; ++i) any |= (p->owner[i] == rank);
+  if (!any) return CZ_OK;   // an empty shard: nothing to do
+  st = check_device();
+  if (st != CZ_OK) return st;
+
+  size_t need = 0;
+  st = cz_workspace_size(plan, rank, shapes, &need);
+  if (st != CZ_OK) return st;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  void* ws = opts->workspace;
+  if (ws) {
+    if (opts->workspace_bytes < need) return CZ_ERR_NOMEM;
+    if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return CZ_ERR_INVALID;
+  } else {
+    st = get_internal_ws(need, &ws);
+    if (st != CZ_OK) return st;
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  Key k;
+  k.plan = plan; k.rank = rank; k.dev = dev;
+  k.param = flat_param; k.grad = flat_grad; k.mom = flat_mom;
+  k.pbf16 = opts->param_bf16; k.dbg = opts->debug_update_out; k.ws = ws;
+  k.grad_bf16 = opts->grad_is_bf16; k.nesterov = opts->nesterov; k.ns_steps = 0;
+  k.lr = lr; k.mu = mu; k.eps = opts->eps; k.a = opts->a; k.b = opts->b; k.c = opts->c;
+  k.offsets.assign(offsets, offsets + p->n_params);
+  k.shapes.assign(shapes, shapes + 2 * p->n_params);
+  std::shared_ptr<Program> prog;
+  auto it = g_cache.find(k);
+  if (it != g_cache.end()) {
+    prog = it->second;
+  } else {
+    prog = std::make_shared<Program>();
+    st = build_program(p, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, *opts,
+                       static_cast<uint8_t*>(ws), *prog);
+    if (st != CZ_OK) return st;
+    if (g_cache.size() > 64) g_cache.clear();
+    g_cache.emplace(k, prog);
+  }
+  // (re)upload the tables if another program used this workspace since
+  auto rk = std::make_pair(dev, (const void*)ws);
+  auto rit = g_resident.find(rk);
+  if (rit == g_resident.end() || rit->second != prog.get()) {
+    if (cudaMemcpyAsync(static_cast<uint8_t*>(ws) + prog->tables_begin, prog->host_tables.data(),
+                        prog->host_tables.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return CZ_ERR_CUDA;
+    g_resident[rk] = prog.get();
+  }
+
+  const Program& P = *prog;
+  if (traced(0, s, [&] { return launch_momentum(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+  if (traced(1, s, [&] { return launch_sigma_finalize(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+  GemmParams gp;
+  for (int t = 0; t < ns_steps; ++t) {
+    const int first = t == 0 ? 1 : 0;
+    const int cur = t & 1;
+    for (const Launch& ln : P.gram) {
+      gp = ln.params;
+      gp.first = first;
+      if (traced(2, s, [&] { return launch_ns_gemm(kGram, gp, P.grid, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+    }
+    for (const Launch& ln : P.poly) {
+      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, ln.params, P.grid, s); }) != cudaSuccess)
+        return CZ_ERR_CUDA;
+    }
+    const bool final_step = t + 1 == ns_steps;
+    const std::vector<Launch>& last = final_step ? P.apply[cur] : P.update[cur];
+    for (const Launch& ln : last) {
+      gp = ln.params;
+      gp.first = first;
+      if (traced(final_step ? 5 : 4, s, [&] { return launch_ns_gemm(ln.phase, gp, P.grid, s); }) != cudaSuccess)
+        return CZ_ERR_CUDA;
+    }
+  }
+  return CZ_OK;
+}
+
+int cz_device_status(void* stream, void* workspace, int* status_out) {
+  if (!status_out) return CZ_ERR_INVALID;
+  *status_out = CZ_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CZ_ERR_CUDA;
+  void* ws = workspace;
+  if (!ws) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CZ_ERR_CUDA;
+    auto it = g_ws.find(dev);
+    if (it == g_ws.end() || !it->second.ptr) return CZ_OK;
+    ws = it->second.ptr;
+  }
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CZ_ERR_CUDA;
+  if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return CZ_ERR_CUDA;
+  *status_out = v;
+  return CZ_OK;
+}
+
+int cz_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return CZ_OK;
+}
+
+int cz_profile_read(double* ms, int64_t* launches, int32_t n_kinds) {
+  if (!ms || !launches || n_kinds < 0 || n_kinds > CZ_KERNEL_KINDS) return CZ_ERR_INVALID;
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  for (int i = 0; i < n_kinds; ++i) {
+    ms[i] = 0.0;
+    launches[i] = 0;
+  }
+  int st = CZ_OK;
+  for (ProfRec& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) st = CZ_ERR_CUDA;
+    if (r.kind < n_kinds) {
+      ms[r.kind] += t;
+      launches[r.kind] += 1;
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  return st;
+}
+
+const char* cz_status_string(int status) {
+  switch (status) {
+    case CZ_OK: return "ok";
+    case CZ_ERR_INVALID: return "invalid argument";
+    case CZ_ERR_CUDA: return "CUDA call failed";
+    case CZ_ERR_NOMEM: return "out of memory / workspace too small";
+    case CZ_ERR_PLAN_MISMATCH: return "offsets/shapes do not match the plan";
+    case CZ_ERR_TIMEOUT: return "device-side wait timed out";
+    case CZ_ERR_DEVICE_CHECK: return "device-side check failed";
+    case CZ_ERR_UNSUPPORTED: return "unsupported device or feature";
+    default: return "unknown status";
+  }
+}
+
+const char* cz_version(void) { return "cz 0.1 sm_103a"; }
+
+}  // extern "C"

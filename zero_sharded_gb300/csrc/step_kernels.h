@@ -1,0 +1,114 @@
+// Launch interface between the host orchestration of the Muon step
+// (muon_step.cpp) and the CUDA kernels (momentum.cu, ns_gemm.cu).
+// Plain structs with device pointers; bf16 buffers are uint16_t on the host side.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cz {
+
+// ------------------------------------------------------------------ momentum pass
+// One 64 x 64 tile of one owned tensor (rows x cols layout of the parameter).
+struct MomTile {
+  int32_t mat;     // index into MomMat
+  int32_t r0, c0;  // tile origin (element row / column)
+  int32_t pad;
+};
+
+struct MomMat {
+  int64_t off;            // element offset of the tensor in the flat buffers
+  int32_t rows, cols;     // parameter layout (rows x cols, row-major)
+  uint16_t* direct;       // bf16 buffer receiving u in rows x cols orientation
+  uint16_t* trans;        // bf16 buffer receiving u^T (cols x rows)
+  int64_t ld_direct;      // element pitch of `direct` rows
+  int64_t ld_trans;       // element pitch of `trans` rows
+  int32_t tile_first;     // first tile of this tensor (its partial sums are contiguous)
+  int32_t tile_count;
+};
+
+struct MomParams {
+  float* mom;             // flat fp32 momentum
+  const void* grad;       // flat fp32 or bf16 gradient
+  int32_t grad_bf16;
+  int32_t nesterov;
+  float mu;
+  float eps;
+  const MomTile* tiles;
+  int32_t n_tiles;
+  const MomMat* mats;
+  int32_t n_mats;
+  float* partial;         // per tile: sum of u^2 over the tile
+  float* sigma;           // per tensor: 1 / (||u||_F + eps)
+  int* status;
+};
+
+cudaError_t launch_momentum(const MomParams& p, cudaStream_t s);
+cudaError_t launch_sigma_finalize(const MomParams& p, cudaStream_t s);
+
+// ------------------------------------------------------------------ NS GEMM
+constexpr int kBM = 128;        // UMMA M (TMEM lanes)
+constexpr int kBN = 256;        // UMMA N (TMEM columns per accumulator)
+constexpr int kBK = 64;         // 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kMaxProblems = 16;
+
+enum Phase : int32_t {
+  kGram = 0,     // A = s^2 X X^T            (symmetric output)
+  kPoly = 1,     // B = b A + c A A          (symmetric output)
+  kUpdate = 2,   // X <- s (a X + B X), also writes X^T
+  kApply = 3,    // last step: W <- W - lr*scale*s(a X + B X)  (+ bf16 copy, debug delta)
+};
+
+// One batched GEMM: `count` matrices of the same M x N x K, operands read by
+// the two tensor maps of the same index (A side: M rows, B side: N rows, both
+// K-major), output written by the epilogue of the launch's phase.
+struct GemmProblem {
+  int32_t M, N, K, count;
+  int32_t mat_base;       // global index (sigma / MatInfo) of matrix 0 of this problem
+  int32_t orient;         // kApply: 0 -> output is X (m x n), 1 -> output is X^T (n x m)
+  int32_t pad0, pad1;
+  uint16_t* out;         int64_t ld_out, ms_out;     // element pitch, per-matrix stride
+  uint16_t* out_t;       int64_t ld_out_t, ms_out_t; // kUpdate: X^T written here
+  const uint16_t* aux;   int64_t ld_aux, ms_aux;     // kPoly: A; kUpdate/kApply: current X (or X^T)
+};
+
+// Per global matrix: where its parameter lives (for the apply epilogue).
+struct MatInfo {
+  int64_t w_off;          // element offset in the flat parameter buffers
+  int32_t rows, cols;     // parameter layout
+  float lrs;              // lr * sqrt(max(1, rows/cols))
+  int32_t vec_ok;         // w_off and cols are multiples of 4 (16-byte fp32 vectors)
+};
+
+struct GemmParams {
+  CUtensorMap tmA[kMaxProblems];
+  CUtensorMap tmB[kMaxProblems];
+  GemmProblem prob[kMaxProblems];
+  int32_t n_prob;
+  int32_t n_tiles;
+  const int4* tiles;      // {problem, matrix, tile_m, tile_n}
+  const float* sigma;     // per global matrix
+  const MatInfo* mats;    // per global matrix
+  float a, b, c;
+  int32_t first;          // 1: Newton-Schulz step 1 (scale by sigma)
+  float* W;               // fp32 master (kApply)
+  uint16_t* Wb;           // bf16 copy or null (kApply)
+  float* dbg;             // debug delta or null (kApply)
+  int* status;
+  int64_t timeout_ns;
+};
+
+// Dynamic shared memory of the GEMM kernel.
+constexpr int kStageBytesA = kBM * kBK * 2;
+constexpr int kStageBytesB = kBN * kBK * 2;
+constexpr int kEpiPitch = 40;                                 // bf16 per transpose row (32 + 8 pad)
+constexpr int kEpiBytesPerWarp = 32 * kEpiPitch * 2;
+constexpr int kGemmSmemBytes =
+    1024 /*align slack*/ + kStages * (kStageBytesA + kStageBytesB) + 4 * kEpiBytesPerWarp + 256 /*barriers*/;
+
+cudaError_t launch_ns_gemm(int phase, const GemmParams& p, int grid, cudaStream_t s);
+int gemm_max_grid();   // SM count of the current device (persistent grid bound)
+
+}  // namespace cz
