@@ -319,7 +319,9 @@ def main():
     ns_tflops = F / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0
     peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
     el = sum(r * c for r, c in my_shapes)
-    mom_bytes = el * (12 + (2 if w.grad_bf16 else 4))          # read g, m; write m, bf16 X
+    # algorithmic bytes of the momentum pass: read g and m, write m and one bf16 copy of u
+    mom_bytes = el * (10 + (2 if w.grad_bf16 else 4))
+    mom_moved = mom_bytes + 2 * el                             # this design also writes u^T (bf16)
     mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9 if mom_ms > 0 else 0.0
     hbm = float(peaks.get("hbm_gbs", 6800.0))
 
@@ -371,6 +373,7 @@ def main():
                          "launches_per_step": ns_launch, "ms_per_step": ns_ms},
             "momentum_pass": {"bound": "hbm", "achieved": mom_gbs, "peak": hbm, "unit": "GB/s",
                               "frac": mom_gbs / hbm if hbm else None, "bytes_per_element": mom_bytes / max(el, 1),
+                              "moved_bytes_per_element": mom_moved / max(el, 1),
                               "ms_per_step": mom_ms, "peak_source": f"hbm_gbs of {peak_src}"},
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
             "cpu_baseline": cpu, "e2e": e2e,

@@ -12,7 +12,12 @@ struct cz_plan {};   // the opaque handle type of the C-ABI; cz::Plan derives fr
 
 namespace cz {
 
+// Process-unique id for plans and step programs: caches key on it, never on
+// an address that a later allocation could reuse.
+uint64_t next_uid();
+
 struct Plan : cz_plan {
+  uint64_t uid = next_uid();
   int32_t R = 1;
   int64_t n_params = 0, n_buckets = 0;
   int kind = 0;              // 0: Algorithm 1, 1: Eq. 1 start-index split

@@ -191,6 +191,7 @@ struct Launch {
 
 // Everything that depends only on (plan, rank, shapes, offsets, buffers, options).
 struct Program {
+  uint64_t uid = next_uid();
   Layout L;
   std::vector<uint8_t> host_tables;   // image of [off_sigma .. off_tiles + tiles) region (tables only)
   int64_t tables_begin = 0, tables_end = 0;
@@ -200,7 +201,7 @@ struct Program {
 };
 
 struct Key {
-  const void* plan; int32_t rank; int dev;
+  uint64_t plan; int32_t rank; int dev;
   const void *param, *grad, *mom, *pbf16, *dbg, *ws;
   int32_t grad_bf16, nesterov, ns_steps;
   float lr, mu, eps, a, b, c;
@@ -235,7 +236,7 @@ cudaError_t traced(int kind, cudaStream_t s, F&& fn) {
 
 std::mutex g_mu;
 std::map<Key, std::shared_ptr<Program>> g_cache;
-std::map<std::pair<int, const void*>, const Program*> g_resident;   // tables currently uploaded per workspace
+std::map<std::pair<int, const void*>, uint64_t> g_resident;   // program whose tables a workspace holds
 struct DevWs { void* ptr = nullptr; size_t bytes = 0; };
 std::map<int, DevWs> g_ws;
 
@@ -579,7 +580,7 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   Key k;
-  k.plan = plan; k.rank = rank; k.dev = dev;
+  k.plan = p->uid; k.rank = rank; k.dev = dev;
   k.param = flat_param; k.grad = flat_grad; k.mom = flat_mom;
   k.pbf16 = opts->param_bf16; k.dbg = opts->debug_update_out; k.ws = ws;
   k.grad_bf16 = opts->grad_is_bf16; k.nesterov = opts->nesterov; k.ns_steps = 0;
@@ -601,11 +602,11 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
   // (re)upload the tables if another program used this workspace since
   auto rk = std::make_pair(dev, (const void*)ws);
   auto rit = g_resident.find(rk);
-  if (rit == g_resident.end() || rit->second != prog.get()) {
+  if (rit == g_resident.end() || rit->second != prog->uid) {
     if (cudaMemcpyAsync(static_cast<uint8_t*>(ws) + prog->tables_begin, prog->host_tables.data(),
                         prog->host_tables.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
       return CZ_ERR_CUDA;
-    g_resident[rk] = prog.get();
+    g_resident[rk] = prog->uid;
   }
 
   const Program& P = *prog;

@@ -9,12 +9,20 @@
 #include "cz_internal.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <new>
 #include <numeric>
 #include <vector>
 
 using cz::Plan;
+
+namespace cz {
+uint64_t next_uid() {
+  static std::atomic<uint64_t> counter{1};
+  return counter.fetch_add(1);
+}
+}  // namespace cz
 
 namespace {
 
