@@ -249,7 +249,7 @@ def main():
     M = torch.zeros_like(P)
     PB = P.to(torch.bfloat16)
     ws_bytes = cz.cz_workspace_size(plan, my_rank, w.shapes)
-    WS = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    WS = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)   # status word starts at zero
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MiB > 129 MB L2
     sargs = cz.StepArgs(w.offsets, w.shapes)
     opts = cz.make_opts(param_bf16=PB, workspace=WS, workspace_bytes=ws_bytes, grad_is_bf16=w.grad_bf16)

@@ -105,7 +105,9 @@ typedef struct {
   void*   param_bf16;      /* nullable: bf16 copy of the parameters, same flat layout;
                               written as RNE(new fp32 master) for owned tensors        */
   void*   workspace;       /* nullable: caller-owned device scratch of workspace_bytes
-                              (>= cz_workspace_size).  NULL: the library's cached one  */
+                              (>= cz_workspace_size, 256-byte aligned; its first 256
+                              bytes -- the status word -- must be zero before first
+                              use).  NULL: the library's cached one                     */
   size_t  workspace_bytes;
   float*  debug_update_out;/* nullable: fp32 flat buffer (param layout); receives
                               lr*sqrt(max(1,rows/cols))*X_K for owned tensors          */
@@ -144,6 +146,31 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank,
                     const int64_t* offsets, const int64_t* shapes,
                     float lr, float mu, int32_t ns_steps, void* stream,
                     const cz_step_opts* opts);
+
+/* cz_muon_step without any device allocation.  The paper has no counterpart
+ * to this call; it exists for callers that cannot call cudaMalloc when they run
+ * the step (an allocator that owns all device memory, memory reserved up front,
+ * or code that must avoid the synchronisation cudaMalloc/cudaFree can cause).
+ * Same arguments, kernels and results as cz_muon_step_ex; the workspace is a
+ * static device array of CZ_STATIC_WORKSPACE_BYTES (64 MiB) that every GPU
+ * loading the library holds until the process exits.
+ *   - opts may be NULL (defaults); opts->workspace must be NULL and
+ *     workspace_bytes 0, else CZ_ERR_INVALID.
+ *   - A shard whose cz_workspace_size exceeds CZ_STATIC_WORKSPACE_BYTES is
+ *     rejected with CZ_ERR_NOMEM before any GPU work.
+ *   - The first call on each device does a set-up (looks up the array's device
+ *     address and clears its status word, synchronously); make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race.  Device-side errors are recorded in the
+ *     array's status word and are not reported by this call.
+ * Calls no cudaMalloc, cudaFree or other allocating routine. */
+#define CZ_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank,
+                         float* flat_param, const void* flat_grad, float* flat_mom,
+                         const int64_t* offsets, const int64_t* shapes,
+                         float lr, float mu, int32_t ns_steps, void* stream,
+                         const cz_step_opts* opts);
 
 /* Synchronises `stream`, reads and clears the device status word kept in
  * `workspace` (NULL: the library's cached workspace of the current device).

@@ -193,3 +193,22 @@ def test_deterministic_repeat():
     b.step()
     assert torch.equal(a.P.cpu(), b.P.cpu())
     assert torch.equal(a.D.cpu(), b.D.cpu())
+
+
+def test_caller_workspace_reused_between_calls():
+    """A caller workspace whose memory is overwritten between calls (as when an
+    allocator hands the same block to another tensor) gives the same results as
+    the library's own workspace: the step re-sends its tables on every call."""
+    shapes = [(256, 768), (768, 256), (128, 128)]
+    a = Run(shapes, R=1, seed=23)
+    b = Run(shapes, R=1, seed=23)
+    ws_bytes = cz.cz_workspace_size(a.plan, 0, shapes)
+    WS = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    for call in range(2):
+        a.step()
+        opts = cz.make_opts(param_bf16=b.PB, debug_update_out=b.D, workspace=WS, workspace_bytes=ws_bytes)
+        cz.cz_muon_step_ex(b.plan, 0, b.P, b.G, b.M, b.args, LR, MU, 5, None, opts)
+        assert cz.cz_device_status(None, WS) == cz.CZ_OK
+        assert torch.equal(a.P.cpu(), b.P.cpu())
+        assert torch.equal(a.M.cpu(), b.M.cpu())
+        WS[256:].fill_(0xA5)        # scribble over everything but the status word

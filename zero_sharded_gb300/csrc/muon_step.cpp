@@ -236,7 +236,6 @@ cudaError_t traced(int kind, cudaStream_t s, F&& fn) {
 
 std::mutex g_mu;
 std::map<Key, std::shared_ptr<Program>> g_cache;
-std::map<std::pair<int, const void*>, uint64_t> g_resident;   // program whose tables a workspace holds
 struct DevWs { void* ptr = nullptr; size_t bytes = 0; };
 std::map<int, DevWs> g_ws;
 
@@ -599,15 +598,12 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
     if (g_cache.size() > 64) g_cache.clear();
     g_cache.emplace(k, prog);
   }
-  // (re)upload the tables if another program used this workspace since
-  auto rk = std::make_pair(dev, (const void*)ws);
-  auto rit = g_resident.find(rk);
-  if (rit == g_resident.end() || rit->second != prog->uid) {
-    if (cudaMemcpyAsync(static_cast<uint8_t*>(ws) + prog->tables_begin, prog->host_tables.data(),
-                        prog->host_tables.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return CZ_ERR_CUDA;
-    g_resident[rk] = prog->uid;
-  }
+  // The tables (tile lists, per-tensor descriptors) are copied into the
+  // workspace on every call: the caller may have reused the workspace memory
+  // for something else since the last call, even at the same address.
+  if (cudaMemcpyAsync(static_cast<uint8_t*>(ws) + prog->tables_begin, prog->host_tables.data(),
+                      prog->host_tables.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return CZ_ERR_CUDA;
 
   const Program& P = *prog;
   if (traced(0, s, [&] { return launch_momentum(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
