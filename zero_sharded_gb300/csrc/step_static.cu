@@ -1,0 +1,80 @@
+// cz_muon_step_noalloc: the Muon step with its scratch in a static device array.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// optimizer step: a framework whose caching allocator owns all of device memory
+// and forbids side allocations, a runtime that reserves memory up front and
+// treats any later cudaMalloc as an error, or an embedding that must not trigger
+// the implicit device synchronisation that cudaMalloc/cudaFree can cause.  For
+// them this entry point runs exactly the same kernels as cz_muon_step_ex, but
+// the workspace is the file-scope array below, so the call allocates nothing:
+// no cudaMalloc, no cudaFree, no allocating library routine.
+//
+// The array holds CZ_STATIC_WORKSPACE_BYTES on every GPU that loads the library,
+// for the life of the process.  Every call shares it and it keeps the previous
+// call's contents: the kernels overwrite everything they read except the status
+// word, which is cleared once per device at set-up.  Calls that overlap on the
+// GPU (different streams, or different host threads without ordering) race on
+// the array.
+
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+
+#include "cz.h"
+#include "cz_internal.h"
+
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[CZ_STATIC_WORKSPACE_BYTES];
+
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_ptr;   // per device: device address of g_noalloc_scratch
+
+// Set-up, once per device, with that device current: the host name of the
+// array is only a stand-in, so its device address is looked up here and passed
+// on as the workspace pointer.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CZ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  auto it = g_noalloc_ptr.find(dev);
+  if (it == g_noalloc_ptr.end()) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return CZ_ERR_CUDA;
+    }
+    // the status word (first bytes of the workspace header) must start at zero
+    if (cudaMemset(ptr, 0, 256) != cudaSuccess) return CZ_ERR_CUDA;
+    it = g_noalloc_ptr.emplace(dev, ptr).first;
+  }
+  *out = it->second;
+  return CZ_OK;
+}
+
+}  // namespace
+
+extern "C" int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad,
+                                    float* flat_mom, const int64_t* offsets, const int64_t* shapes, float lr,
+                                    float mu, int32_t ns_steps, void* stream, const cz_step_opts* opts) {
+  if (!plan || !shapes) return CZ_ERR_INVALID;
+  cz_step_opts o;
+  if (opts) {
+    o = *opts;
+    if (o.workspace || o.workspace_bytes) return CZ_ERR_INVALID;   // the scratch is the static array
+  } else {
+    cz_step_opts_default(&o);
+  }
+  size_t need = 0;
+  int st = cz_workspace_size(plan, rank, shapes, &need);
+  if (st != CZ_OK) return st;
+  if (need > (size_t)CZ_STATIC_WORKSPACE_BYTES) return CZ_ERR_NOMEM;   // shard too large for the array
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != CZ_OK) return st;
+  o.workspace = scratch;
+  o.workspace_bytes = (size_t)CZ_STATIC_WORKSPACE_BYTES;
+  return cz_muon_step_ex(plan, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, stream, &o);
+}

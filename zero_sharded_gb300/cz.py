@@ -86,6 +86,9 @@ def load() -> ctypes.CDLL:
         "cz_muon_step_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_void_p, _i64p, _i64p, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER(cz_step_opts)]),
+        "cz_muon_step_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, _i64p, _i64p, ctypes.c_float, ctypes.c_float,
+                                                ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER(cz_step_opts)]),
         "cz_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, _i32p]),
         "cz_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
         "cz_profile_read": (ctypes.c_int, [_f64p, _i64p, ctypes.c_int32]),
@@ -249,6 +252,18 @@ def cz_muon_step_ex(plan: Plan, rank: int, flat_param, flat_grad, flat_mom, args
                                 args.offsets, args.shapes, float(lr), float(mu), int(ns_steps), _stream_ptr(stream),
                                 ctypes.byref(opts))
     _check("cz_muon_step_ex", st)
+
+
+CZ_STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024
+
+
+def cz_muon_step_noalloc(plan: Plan, rank: int, flat_param, flat_grad, flat_mom, args: StepArgs, lr: float,
+                         mu: float, ns_steps: int, stream=None, opts: Optional[cz_step_opts] = None) -> None:
+    """The step with the library's static device scratch: allocates no device memory."""
+    st = load().cz_muon_step_noalloc(plan.handle, int(rank), _ptr(flat_param), _ptr(flat_grad), _ptr(flat_mom),
+                                     args.offsets, args.shapes, float(lr), float(mu), int(ns_steps),
+                                     _stream_ptr(stream), ctypes.byref(opts) if opts is not None else None)
+    _check("cz_muon_step_noalloc", st)
 
 
 def make_opts(param_bf16=None, workspace=None, workspace_bytes: int = 0, debug_update_out=None,
