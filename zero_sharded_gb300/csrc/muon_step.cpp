@@ -167,18 +167,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 3-D bf16 map over `count` matrices of `rows` x `inner` (row pitch ld elements,
-// matrix stride ms elements), box = 64 (inner) x box_rows x 1, 128-byte swizzle.
+// matrix stride ms elements).  Operand loads: box 64 (inner) x box_rows, 128-byte
+// swizzle.  Output stores (store = true): box 32 x 32, no swizzle (dense smem block).
 bool encode_map(CUtensorMap* map, void* base, int64_t inner, int64_t rows, int64_t count, int64_t ld, int64_t ms,
-                uint32_t box_rows) {
+                uint32_t box_rows, bool store = false) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)count};
   cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(ms * 2)};
-  cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1};
+  cuuint32_t box[3] = {store ? 32u : (cuuint32_t)kBK, store ? 32u : box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, store ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -248,7 +249,7 @@ T* at(std::vector<uint8_t>& img, int64_t base, int64_t off) {
 // longest K goes first (LPT), then chunked into launches of <= kMaxProblems problems.
 struct ProbDesc {
   GemmProblem gp;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, to, tot;
   std::vector<int4> tiles;
 };
 
@@ -273,6 +274,8 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
     for (size_t i = c0; i < c1; ++i) {
       ln.params.tmA[i - c0] = probs[i].ta;
       ln.params.tmB[i - c0] = probs[i].tb;
+      ln.params.tmO[i - c0] = probs[i].to;
+      ln.params.tmOT[i - c0] = probs[i].tot;
       ln.params.prob[i - c0] = probs[i].gp;
     }
     ln.params.first = first;
@@ -384,36 +387,37 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b)
           if (a * kBM <= b * kBN + kBN - 1) sym.push_back(make_int4(0, j, (int)a, (int)b));
     {
-      ProbDesc d;
-      std::memset(&d.gp, 0, sizeof(d.gp));
+      // Gram: A = s^2 X X^T, stored with its mirror into A
+      ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.n; d.gp.count = c; d.gp.mat_base = G.mat_base;
-      d.gp.out = A; d.gp.ld_out = G.ldm; d.gp.ms_out = msa;
-      if (!encode_map(&d.ta, X, G.n, G.m, c, G.ldx, msx, kBM) || !encode_map(&d.tb, X, G.n, G.m, c, G.ldx, msx, kBN))
+      if (!encode_map(&d.ta, X, G.n, G.m, c, G.ldx, msx, kBM) || !encode_map(&d.tb, X, G.n, G.m, c, G.ldx, msx, kBN) ||
+          !encode_map(&d.to, A, G.m, G.m, c, G.ldm, msa, 0, true))
         return CZ_ERR_CUDA;
+      d.tot = d.to;
       d.tiles = sym;
       gram.push_back(d);
     }
     {
-      ProbDesc d;
-      std::memset(&d.gp, 0, sizeof(d.gp));
+      // Poly: B' = a I + b A + c A A, stored with its mirror into B
+      ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
-      d.gp.out = B; d.gp.ld_out = G.ldm; d.gp.ms_out = msa;
       d.gp.aux = A; d.gp.ld_aux = G.ldm; d.gp.ms_aux = msa;
-      if (!encode_map(&d.ta, A, G.m, G.m, c, G.ldm, msa, kBM) || !encode_map(&d.tb, A, G.m, G.m, c, G.ldm, msa, kBN))
+      if (!encode_map(&d.ta, A, G.m, G.m, c, G.ldm, msa, kBM) || !encode_map(&d.tb, A, G.m, G.m, c, G.ldm, msa, kBN) ||
+          !encode_map(&d.to, B, G.m, G.m, c, G.ldm, msa, 0, true))
         return CZ_ERR_CUDA;
+      d.tot = d.to;
       d.tiles = sym;
       poly.push_back(d);
     }
     for (int cur = 0; cur < 2; ++cur) {
-      // update: X (m x n) <- a X + B X; operands B rows (K = m) and X^T rows (K = m)
-      ProbDesc d;
-      std::memset(&d.gp, 0, sizeof(d.gp));
+      // update: X (m x n) <- s B' X; operands B' rows (K = m) and X^T rows (K = m);
+      // stores X and X^T (into the other ping-pong buffer)
+      ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.n; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
-      d.gp.out = X; d.gp.ld_out = G.ldx; d.gp.ms_out = msx;
-      d.gp.out_t = XT[cur ^ 1]; d.gp.ld_out_t = G.ldm; d.gp.ms_out_t = mst;
-      d.gp.aux = X; d.gp.ld_aux = G.ldx; d.gp.ms_aux = msx;
       if (!encode_map(&d.ta, B, G.m, G.m, c, G.ldm, msa, kBM) ||
-          !encode_map(&d.tb, XT[cur], G.m, G.n, c, G.ldm, mst, kBN))
+          !encode_map(&d.tb, XT[cur], G.m, G.n, c, G.ldm, mst, kBN) ||
+          !encode_map(&d.to, X, G.n, G.m, c, G.ldx, msx, 0, true) ||
+          !encode_map(&d.tot, XT[cur ^ 1], G.m, G.n, c, G.ldm, mst, 0, true))
         return CZ_ERR_CUDA;
       for (int j = 0; j < c; ++j)
         for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
@@ -423,7 +427,6 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       if (G.has_wide) {
         ProbDesc e = d;
         e.gp.orient = 0;
-        e.gp.out = nullptr; e.gp.out_t = nullptr;
         e.tiles.clear();
         for (int j = 0; j < c; ++j) {
           if (L.mats[G.mat_base + j].tall) continue;
@@ -434,11 +437,9 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       }
       // apply, tall tensors: output X^T (n x m) = parameter layout; operands X^T rows and B rows
       if (G.has_tall) {
-        ProbDesc e;
-        std::memset(&e.gp, 0, sizeof(e.gp));
+        ProbDesc e{};
         e.gp.M = G.n; e.gp.N = G.m; e.gp.K = G.m; e.gp.count = c; e.gp.mat_base = G.mat_base;
         e.gp.orient = 1;
-        e.gp.aux = XT[cur]; e.gp.ld_aux = G.ldm; e.gp.ms_aux = mst;
         if (!encode_map(&e.ta, XT[cur], G.m, G.n, c, G.ldm, mst, kBM) ||
             !encode_map(&e.tb, B, G.m, G.m, c, G.ldm, msa, kBN))
           return CZ_ERR_CUDA;

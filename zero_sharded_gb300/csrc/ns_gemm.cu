@@ -5,26 +5,32 @@
 // "problem"; a launch carries up to kMaxProblems of them and a flat tile list).
 // All products are D = A * B^T with both operands K-major bf16 and an fp32
 // accumulator in TMEM:
-//   Gram    A_t = X X^T                 operands X rows, X rows      (K = n)
-//   Poly    B_t = b A + c A A^T         operands A rows, A rows      (K = m), A symmetric
-//   Update  X  <- a X + B X = a X + B (X^T)^T   operands B rows, X^T rows (K = m)
-// The update also writes X^T for the next step, so no MN-major operand is needed.
-// Step 1 folds the Frobenius normalisation in as scalars: A_1 = s^2 X~X~^T and
-// X_1 = s (a X~ + B_1 X~), s = 1/(||u||_F + eps).  The last update instead runs
-// the apply epilogue: W <- W - lr*sqrt(max(1,rows/cols)) * X_K in fp32, the bf16
-// parameter copy, and (optionally) the applied delta.
+//   Gram    A  = X X^T                  operands X rows, X rows      (K = n)
+//   Poly    B' = a I + b A + c A A^T    operands A rows, A rows      (K = m), A symmetric
+//   Update  X <- B' X = B' (X^T)^T      operands B' rows, X^T rows   (K = m)
+// a X + B X = (a I + B) X, so the a X term rides in the Poly output and the
+// Update epilogue reads no operand.  The Update also writes X^T for the next
+// step, so no MN-major operand is needed.  Step 1 folds the Frobenius
+// normalisation in as scalars: A_1 = s^2 X~X~^T and X_1 = s B'_1 X~,
+// s = 1/(||u||_F + eps).  The last Update instead runs the apply epilogue:
+// W <- W - lr*sqrt(max(1,rows/cols)) * X_K in fp32, the bf16 parameter copy,
+// and (optionally) the applied delta.
 //
 // Structure (one CTA per SM, persistent over a static round-robin tile list):
 //   warp 0      TMA producer: 128x64 (A side) and 256x64 (B side) bf16 tiles,
 //               128-byte swizzle, kStages-deep mbarrier ring
 //   warp 1      TMEM allocation (512 columns = two 128x256 fp32 accumulators)
 //               and the single thread that issues tcgen05.mma (M=128, N=256, K=16)
-//   warps 2..5  epilogue: tcgen05.ld 32 columns at a time from its TMEM lane
-//               quarter, phase-specific math, bf16/fp32 stores; a per-warp smem
-//               transpose writes the mirrored (symmetric) or X^T copy.
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (each takes half of the
+//               tile's 256 columns): tcgen05.ld 32 columns at a time, phase math,
+//               then the 32 x 32 block is staged in smem (as is and transposed)
+//               and written with TMA bulk tensor stores, which clip at the
+//               tensor's edges.  The global operands an epilogue chunk needs
+//               (A for Poly, W for the apply) are loaded one chunk ahead, the
+//               first chunk's before waiting for the accumulator.
 // The TMEM double buffer lets the epilogue of tile i overlap the mainloop of i+1.
 // For the symmetric products only tiles touching the upper triangle are
-// computed; each element (i <= j) is written once directly and once mirrored.
+// computed.
 
 #include <cuda_bf16.h>
 
@@ -35,13 +41,13 @@ namespace cz {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 
 struct Smem {
-  uint8_t* a[kStages];
-  uint8_t* b[kStages];
-  __nv_bfloat16* epi;      // 4 warps x 32 x kEpiPitch
+  uint8_t* a;              // kStages A tiles of kStageBytesA (1024-byte aligned)
+  uint8_t* b;              // kStages B tiles of kStageBytesB
+  __nv_bfloat16* epi;      // kEpiWarps x (direct + transposed 32 x 32 bf16 staging blocks)
   uint64_t* full;          // [kStages]
   uint64_t* empty;         // [kStages]
   uint64_t* tfull;         // [2]
@@ -55,12 +61,12 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   Smem s;
   const uint32_t base = smem_u32(raw);
   uint8_t* p = raw + ((1024u - (base & 1023u)) & 1023u);
-  for (int i = 0; i < kStages; ++i) s.a[i] = p + i * kStageBytesA;
+  s.a = p;
   p += kStages * kStageBytesA;
-  for (int i = 0; i < kStages; ++i) s.b[i] = p + i * kStageBytesB;
+  s.b = p;
   p += kStages * kStageBytesB;
   s.epi = reinterpret_cast<__nv_bfloat16*>(p);
-  p += 4 * kEpiBytesPerWarp;
+  p += kEpiWarps * kEpiBytesPerWarp;
   uint64_t* bars = reinterpret_cast<uint64_t*>(p);
   s.full = bars;
   s.empty = bars + kStages;
@@ -74,180 +80,100 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// bf16 <-> fp32 with register bit operations only (no address-taken temporaries).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
 __device__ __forceinline__ uint4 pack8(const float* v) {
-  uint4 r;
-  __nv_bfloat162 t;
-  t = __floats2bfloat162_rn(v[0], v[1]); r.x = *reinterpret_cast<uint32_t*>(&t);
-  t = __floats2bfloat162_rn(v[2], v[3]); r.y = *reinterpret_cast<uint32_t*>(&t);
-  t = __floats2bfloat162_rn(v[4], v[5]); r.z = *reinterpret_cast<uint32_t*>(&t);
-  t = __floats2bfloat162_rn(v[6], v[7]); r.w = *reinterpret_cast<uint32_t*>(&t);
-  return r;
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
 }
 
 __device__ __forceinline__ void unpack8(uint4 r, float* v) {
-  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-    v[2 * i] = __low2float(t);
-    v[2 * i + 1] = __high2float(t);
-  }
+  v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x);
+  v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
+  v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z);
+  v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
 }
 
-// 32 bf16 of row `row`, columns [col0, col0+32) of a bf16 matrix (row pitch ld);
-// vectors starting at or beyond `ncols` read as zero.
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* base, int64_t ld, int row, int col0, int ncols,
-                                           float* v) {
-  const __nv_bfloat16* p = base + (int64_t)row * ld + col0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (col0 + q * 8 < ncols) {
-      unpack8(*reinterpret_cast<const uint4*>(p + q * 8), v + q * 8);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[q * 8 + e] = 0.f;
-    }
-  }
-}
-
-// Direct store of 32 values at (row, col0..col0+31).  SYM: only elements with
-// col >= row are stored (the upper triangle incl. the diagonal).
-template <bool SYM>
-__device__ __forceinline__ void store_row32(__nv_bfloat16* base, int64_t ld, int row, int col0, int ncols,
-                                            const float* v) {
-  __nv_bfloat16* p = base + (int64_t)row * ld + col0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int c8 = col0 + q * 8;
-    if (c8 >= ncols) continue;
-    if (!SYM || c8 >= row) {
-      *reinterpret_cast<uint4*>(p + q * 8) = pack8(v + q * 8);
-    } else if (c8 + 7 >= row) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (c8 + e >= row && c8 + e < ncols) p[q * 8 + e] = __float2bfloat16_rn(v[q * 8 + e]);
-    }
-  }
-}
-
-// Transposed store through the warp's smem scratch: the warp holds rows
-// [rbase, rbase+32) x columns [col0, col0+32); lane L writes row col0+L of the
-// target, columns [rbase, rbase+32).  SYM: only source elements with row < col
-// (their mirror lies strictly below the diagonal).  nrows/ncols bound the
-// source tile; the caller guarantees col0 < ncols.
-template <bool SYM>
-__device__ __forceinline__ void store_transposed32(__nv_bfloat16* scratch, __nv_bfloat16* base, int64_t ld,
-                                                   int rbase, int col0, int nrows, int ncols, const float* v,
-                                                   int lane) {
-#pragma unroll
-  for (int q = 0; q < 32; ++q) scratch[q * kEpiPitch + lane] = __float2bfloat16_rn(v[q]);
-  __syncwarp();
-  const int trow = col0 + lane;          // target row = source column
-  if (trow < ncols) {
-    __nv_bfloat16* p = base + (int64_t)trow * ld + rbase;
-    const __nv_bfloat16* s = scratch + lane * kEpiPitch;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r8 = rbase + q * 8;      // source rows r8..r8+7
-      if (r8 >= nrows) continue;
-      const bool full = !SYM || (r8 + 7 < trow);
-      if (full) {
-        *reinterpret_cast<uint4*>(p + q * 8) = *reinterpret_cast<const uint4*>(s + q * 8);
-      } else if (r8 < trow) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (r8 + e < trow && r8 + e < nrows) p[q * 8 + e] = s[q * 8 + e];
-      }
-    }
-  }
-  __syncwarp();
-}
+// Operands one epilogue chunk needs from global memory, loaded ahead of use.
+struct Pre {
+  uint4 x[4];     // 32 bf16 of A in this row (Poly: the b A term)
+  float4 w[8];    // 32 fp32 master weights (Apply)
+};
 
 template <int PHASE>
-__device__ __forceinline__ void epilogue_chunk(const GemmParams& p, const GemmProblem& pr, int mat, int row,
-                                               int rbase, int col0, float* v, __nv_bfloat16* scratch,
-                                               int lane) {
-  const int gm = pr.mat_base + mat;
-  const bool row_ok = row < pr.M;
-  if (PHASE == kGram) {
-    float s2 = 1.f;
-    if (p.first) {
-      const float s = p.sigma[gm];
-      s2 = s * s;
+__device__ __forceinline__ void prefetch(Pre& pre, const GemmParams& p, const GemmProblem& pr, int mat, int64_t wrow,
+                                         bool vec_w, int row, bool row_ok, int col0) {
+  if constexpr (PHASE == kPoly) {
+    const __nv_bfloat16* aux = reinterpret_cast<const __nv_bfloat16*>(pr.aux) + (int64_t)mat * pr.ms_aux +
+                               (int64_t)row * pr.ld_aux + col0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      pre.x[q] = (row_ok && col0 + q * 8 < pr.N) ? *reinterpret_cast<const uint4*>(aux + q * 8)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if constexpr (PHASE == kApply) {
+    if (row_ok && vec_w && col0 + 32 <= pr.N) {
+      const float4* W = reinterpret_cast<const float4*>(p.W + wrow + col0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) pre.w[q] = W[q];
     }
+  }
+}
+
+// Writes the warp's 32 x 32 block (lane L holds row L) into dense smem staging:
+// D[L][c] for the direct store and, if wanted, T[c][L] for the transposed one.
+__device__ __forceinline__ void stage_block(__nv_bfloat16* D, __nv_bfloat16* T, const float* v, int lane,
+                                            bool want_t) {
+  uint4* d = reinterpret_cast<uint4*>(D + lane * 32);
 #pragma unroll
-    for (int q = 0; q < 32; ++q) v[q] *= s2;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(pr.out) + (int64_t)mat * pr.ms_out;
-    if (row_ok) store_row32<true>(out, pr.ld_out, row, col0, pr.N, v);
-    store_transposed32<true>(scratch, out, pr.ld_out, rbase, col0, pr.M, pr.N, v, lane);
-  } else if (PHASE == kPoly) {
-    float a[32];
-    const __nv_bfloat16* aux = reinterpret_cast<const __nv_bfloat16*>(pr.aux) + (int64_t)mat * pr.ms_aux;
-    if (row_ok) {
-      load_row32(aux, pr.ld_aux, row, col0, pr.N, a);
-    } else {
+  for (int q = 0; q < 4; ++q) d[q] = pack8(v + 8 * q);
+  if (want_t) {
 #pragma unroll
-      for (int q = 0; q < 32; ++q) a[q] = 0.f;
+    for (int c = 0; c < 32; ++c) T[c * 32 + lane] = __float2bfloat16_rn(v[c]);
+  }
+}
+
+// Apply epilogue of one 32-column chunk: W <- W - lrs * v in the parameter's
+// rows x cols layout, the bf16 copy and the optional debug delta.
+__device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProblem& pr, const MatInfo& mi, int row,
+                                            int col0, float* v, const Pre& pre) {
+  if (row >= pr.M) return;
+  const int64_t wrow = mi.w_off + (int64_t)row * mi.cols;
+  const float lrs = mi.lrs;
+  if (mi.vec_ok && col0 + 32 <= pr.N) {
+    float4* W = reinterpret_cast<float4*>(p.W + wrow + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      float4 w = pre.w[q];
+      const float d0 = lrs * v[4 * q], d1 = lrs * v[4 * q + 1], d2 = lrs * v[4 * q + 2], d3 = lrs * v[4 * q + 3];
+      w.x -= d0; w.y -= d1; w.z -= d2; w.w -= d3;
+      W[q] = w;
+      if (p.dbg) reinterpret_cast<float4*>(p.dbg + wrow + col0)[q] = make_float4(d0, d1, d2, d3);
+      v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
     }
+    if (p.Wb) {
+      uint2* wb = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.Wb) + wrow + col0);
 #pragma unroll
-    for (int q = 0; q < 32; ++q) v[q] = fmaf(p.b, a[q], p.c * v[q]);
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(pr.out) + (int64_t)mat * pr.ms_out;
-    if (row_ok) store_row32<true>(out, pr.ld_out, row, col0, pr.N, v);
-    store_transposed32<true>(scratch, out, pr.ld_out, rbase, col0, pr.M, pr.N, v, lane);
+      for (int q = 0; q < 8; ++q)      // 8-byte stores: wrow + col0 is a multiple of 4 elements
+        wb[q] = make_uint2(pack_bf16x2(v[4 * q], v[4 * q + 1]), pack_bf16x2(v[4 * q + 2], v[4 * q + 3]));
+    }
   } else {
-    // X_new = s * (a X + acc)
-    float x[32];
-    const __nv_bfloat16* aux = reinterpret_cast<const __nv_bfloat16*>(pr.aux) + (int64_t)mat * pr.ms_aux;
-    if (row_ok) {
-      load_row32(aux, pr.ld_aux, row, col0, pr.N, x);
-    } else {
+    float* W = p.W + wrow + col0;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) x[q] = 0.f;
-    }
-    const float s = p.first ? p.sigma[gm] : 1.f;
-#pragma unroll
-    for (int q = 0; q < 32; ++q) v[q] = s * fmaf(p.a, x[q], v[q]);
-    if (PHASE == kUpdate) {
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(pr.out) + (int64_t)mat * pr.ms_out;
-      if (row_ok) store_row32<false>(out, pr.ld_out, row, col0, pr.N, v);
-      __nv_bfloat16* outt = reinterpret_cast<__nv_bfloat16*>(pr.out_t) + (int64_t)mat * pr.ms_out_t;
-      store_transposed32<false>(scratch, outt, pr.ld_out_t, rbase, col0, pr.M, pr.N, v, lane);
-    } else {
-      // apply: the output orientation is the parameter's rows x cols layout
-      if (!row_ok) return;
-      const MatInfo mi = p.mats[gm];
-      const int64_t wrow = mi.w_off + (int64_t)row * mi.cols;
-      float* W = p.W + wrow + col0;
-      const float lrs = mi.lrs;
-      if (mi.vec_ok && col0 + 32 <= pr.N) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float4 w = *reinterpret_cast<const float4*>(W + 4 * q);
-          float d0 = lrs * v[4 * q], d1 = lrs * v[4 * q + 1], d2 = lrs * v[4 * q + 2], d3 = lrs * v[4 * q + 3];
-          w.x -= d0; w.y -= d1; w.z -= d2; w.w -= d3;
-          *reinterpret_cast<float4*>(W + 4 * q) = w;
-          v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
-          if (p.dbg) *reinterpret_cast<float4*>(p.dbg + wrow + col0 + 4 * q) = make_float4(d0, d1, d2, d3);
-        }
-        if (p.Wb) {
-          __nv_bfloat16* wb = reinterpret_cast<__nv_bfloat16*>(p.Wb) + wrow + col0;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 pk = pack8(v + 8 * q);
-            // 8-byte stores: wrow + col0 is a multiple of 4 elements
-            reinterpret_cast<uint2*>(wb + 8 * q)[0] = make_uint2(pk.x, pk.y);
-            reinterpret_cast<uint2*>(wb + 8 * q)[1] = make_uint2(pk.z, pk.w);
-          }
-        }
-      } else {
-        for (int q = 0; q < 32; ++q) {
-          if (col0 + q >= pr.N) break;
-          const float d = lrs * v[q];
-          const float w = W[q] - d;
-          W[q] = w;
-          if (p.dbg) p.dbg[wrow + col0 + q] = d;
-          if (p.Wb) reinterpret_cast<__nv_bfloat16*>(p.Wb)[wrow + col0 + q] = __float2bfloat16_rn(w);
-        }
+    for (int q = 0; q < 32; ++q) {
+      if (col0 + q < pr.N) {
+        const float d = lrs * v[q];
+        const float w = W[q] - d;
+        W[q] = w;
+        if (p.dbg) p.dbg[wrow + col0 + q] = d;
+        if (p.Wb) reinterpret_cast<__nv_bfloat16*>(p.Wb)[wrow + col0 + q] = __float2bfloat16_rn(w);
       }
     }
   }
@@ -268,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tfull[i], 1);
-      mbar_init(&sm.tempty[i], 128);
+      mbar_init(&sm.tempty[i], 32 * kEpiWarps);
     }
     mbar_init(sm.drain, 1);
     *sm.abort = 0;
@@ -287,10 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       for (int i = 0; i < p.n_prob; ++i) {
         tma_prefetch_desc(&p.tmA[i]);
         tma_prefetch_desc(&p.tmB[i]);
+        if (PHASE != kApply) {
+          tma_prefetch_desc(&p.tmO[i]);
+          tma_prefetch_desc(&p.tmOT[i]);
+        }
       }
     }
-    uint32_t stage = 0, phase = 0, issued = 0;
-    uint32_t last_par[kStages] = {0, 0, 0, 0};
+    uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;   // bit s: parity of stage s's last fill
     bool ok = true;
     for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
       const int4 tl = p.tiles[t];
@@ -303,10 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           w = mbar_wait(&sm.empty[stage], phase ^ 1u, abort, p.status, p.timeout_ns);
           if (w) {
             mbar_arrive_expect_tx(&sm.full[stage], kStageBytesA + kStageBytesB);
-            tma_load_3d(sm.a[stage], ma, &sm.full[stage], kb * kBK, tl.z * kBM, tl.y);
-            tma_load_3d(sm.b[stage], mb, &sm.full[stage], kb * kBK, tl.w * kBN, tl.y);
+            tma_load_3d(sm.a + stage * kStageBytesA, ma, &sm.full[stage], kb * kBK, tl.z * kBM, tl.y);
+            tma_load_3d(sm.b + stage * kStageBytesB, mb, &sm.full[stage], kb * kBK, tl.w * kBN, tl.y);
             issued |= 1u << stage;
-            last_par[stage] = phase;
+            last_par = (last_par & ~(1u << stage)) | (phase << stage);
           }
         }
         if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
@@ -322,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     // every issued copy must land before the CTA may exit
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
-        if (issued & (1u << s)) mbar_wait(&sm.full[s], last_par[s], nullptr, p.status, p.timeout_ns);
+        if (issued & (1u << s)) mbar_wait(&sm.full[s], (last_par >> s) & 1u, nullptr, p.status, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -346,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t a0 = smem_u32(sm.a[stage]);
-          const uint32_t b0 = smem_u32(sm.b[stage]);
+          const uint32_t a0 = smem_u32(sm.a + stage * kStageBytesA);
+          const uint32_t b0 = smem_u32(sm.b + stage * kStageBytesB);
 #pragma unroll
           for (int s = 0; s < kBK / 16; ++s) {
             umma_bf16(d, sdesc_kmajor_sw128(a0 + s * 32), sdesc_kmajor_sw128(b0 + s * 32), idesc,
@@ -375,29 +304,110 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue
+    // Symmetric outputs (Gram, Poly) are written by aligned 32 x 32 blocks: a
+    // block above the diagonal is stored directly and mirrored, a diagonal block
+    // directly only, a block below the diagonal not at all (its mirror comes from
+    // the block above), so each element is written exactly once.
+    constexpr bool kSym = PHASE == kGram || PHASE == kPoly;
+    const int ew = warp - 2;                    // 0 .. kEpiWarps-1
     const int quad = warp & 3;                  // TMEM lane quarter this warp may access
-    __nv_bfloat16* scratch = sm.epi + (warp - 2) * (32 * kEpiPitch);
+    const int half = ew >> 2;                   // which 128 of the 256 accumulator columns
+    __nv_bfloat16* stD = sm.epi + ew * (kEpiBytesPerWarp / 2);
+    __nv_bfloat16* stT = stD + 32 * 32;
+    const uint32_t lane_field = (uint32_t)(quad * 32) << 16;
     uint32_t acc = 0, acc_phase = 0;
+    bool pending = false;                       // bulk stores in flight from the staging blocks
     for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
       const int4 tl = p.tiles[t];
+      const GemmProblem& pr = p.prob[tl.x];
+      const int mat = tl.y;
+      const int gm = pr.mat_base + mat;
+      const int rbase = tl.z * kBM + quad * 32;
+      const int row = rbase + lane;
+      const bool row_ok = row < pr.M;
+      const int ch_first = half * 4;
+      const int col_first = tl.w * kBN + ch_first * 32;
+      // chunks this warp reads from TMEM (warp-uniform bit mask)
+      uint32_t need = 0;
+      if (rbase < pr.M) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int col0 = col_first + c * 32;
+          if (col0 < pr.N && (!kSym || rbase <= col0)) need |= 1u << c;
+        }
+      }
+      const int last = need ? 31 - __clz(need) : -1;
+      float s = 1.f;
+      if (p.first) {
+        const float sg = p.sigma[gm];
+        s = (PHASE == kGram) ? sg * sg : sg;
+      }
+      MatInfo mi{};
+      int64_t wrow = 0;
+      if constexpr (PHASE == kApply) {
+        mi = p.mats[gm];
+        wrow = mi.w_off + (int64_t)row * mi.cols;
+      }
+      Pre cur;
+      const int first_c = need ? __ffs(need) - 1 : 0;
+      if (need) prefetch<PHASE>(cur, p, pr, mat, wrow, mi.vec_ok != 0, row, row_ok, col_first + first_c * 32);
       const bool w = mbar_wait(&sm.tfull[acc], acc_phase, abort, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, w)) break;
       tc_fence_after();
-      const GemmProblem& pr = p.prob[tl.x];
-      const int rbase = tl.z * kBM + quad * 32;
-      const int row = rbase + lane;
-      for (int ch = 0; ch < kBN / 32; ++ch) {
-        const int col0 = tl.w * kBN + ch * 32;
-        if (col0 >= pr.N) break;
-        float v[32];
-        tmem_ld32(tmem_base + acc * (uint32_t)kBN + ch * 32 + ((uint32_t)(quad * 32) << 16), v);
-        epilogue_chunk<PHASE>(p, pr, tl.y, row, rbase, col0, v, scratch, lane);
+      const uint32_t tbase = tmem_base + acc * (uint32_t)kBN + lane_field;
+      if (last < 0) {
+        tc_fence_before();
+        mbar_arrive(&sm.tempty[acc]);
       }
-      tc_fence_before();
-      mbar_arrive(&sm.tempty[acc]);
+      for (int c = first_c; c <= last; ++c) {
+        if (!((need >> c) & 1u)) continue;
+        const int col0 = col_first + c * 32;
+        Pre nxt;
+        const uint32_t later = need >> (c + 1);
+        if (later) prefetch<PHASE>(nxt, p, pr, mat, wrow, mi.vec_ok != 0, row, row_ok, col0 + 32 * __ffs(later));
+        float v[32];
+        tmem_ld32(tbase + (uint32_t)((ch_first + c) * 32), v);
+        if (c == last) {                 // accumulator no longer needed: let the MMA reuse it
+          tc_fence_before();
+          mbar_arrive(&sm.tempty[acc]);
+        }
+        if constexpr (PHASE == kApply) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] *= s;
+          apply_chunk(p, pr, mi, row, col0, v, cur);
+        } else {
+          if constexpr (PHASE == kPoly) {
+            // B' = a I + b A + c (A A)
+            float a[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) unpack8(cur.x[q], a + 8 * q);
+            const bool diag = rbase == col0;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = fmaf(p.b, a[q], p.c * v[q]) + ((diag && q == lane) ? p.a : 0.f);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] *= s;   // Gram: s = sigma^2; Update: s = sigma (step 1)
+          }
+          const bool do_t = !kSym || rbase < col0;
+          if (lane == 0 && pending) bulk_wait_read_all();
+          __syncwarp();
+          stage_block(stD, stT, v, lane, do_t);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&p.tmO[tl.x], stD, col0, rbase, mat);
+            if (do_t) tma_store_3d(&p.tmOT[tl.x], stT, rbase, col0, mat);
+            bulk_commit();
+            pending = true;
+          }
+        }
+        cur = nxt;
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0 && pending) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();

@@ -55,10 +55,10 @@ constexpr int kStages = 4;
 constexpr int kMaxProblems = 16;
 
 enum Phase : int32_t {
-  kGram = 0,     // A = s^2 X X^T            (symmetric output)
-  kPoly = 1,     // B = b A + c A A          (symmetric output)
-  kUpdate = 2,   // X <- s (a X + B X), also writes X^T
-  kApply = 3,    // last step: W <- W - lr*scale*s(a X + B X)  (+ bf16 copy, debug delta)
+  kGram = 0,     // A = s^2 X X^T                   (symmetric output)
+  kPoly = 1,     // B' = a I + b A + c A A          (symmetric output)
+  kUpdate = 2,   // X <- s B' X, also writes X^T     (= s (a X + B X))
+  kApply = 3,    // last step: W <- W - lr*scale*s B' X  (+ bf16 copy, debug delta)
 };
 
 // One batched GEMM: `count` matrices of the same M x N x K, operands read by
@@ -69,9 +69,7 @@ struct GemmProblem {
   int32_t mat_base;       // global index (sigma / MatInfo) of matrix 0 of this problem
   int32_t orient;         // kApply: 0 -> output is X (m x n), 1 -> output is X^T (n x m)
   int32_t pad0, pad1;
-  uint16_t* out;         int64_t ld_out, ms_out;     // element pitch, per-matrix stride
-  uint16_t* out_t;       int64_t ld_out_t, ms_out_t; // kUpdate: X^T written here
-  const uint16_t* aux;   int64_t ld_aux, ms_aux;     // kPoly: A; kUpdate/kApply: current X (or X^T)
+  const uint16_t* aux;   int64_t ld_aux, ms_aux;     // kPoly: A (for the b A term)
 };
 
 // Per global matrix: where its parameter lives (for the apply epilogue).
@@ -83,8 +81,10 @@ struct MatInfo {
 };
 
 struct GemmParams {
-  CUtensorMap tmA[kMaxProblems];
-  CUtensorMap tmB[kMaxProblems];
+  CUtensorMap tmA[kMaxProblems];    // A-side operand loads (128 x 64 boxes, 128-byte swizzle)
+  CUtensorMap tmB[kMaxProblems];    // B-side operand loads (256 x 64 boxes)
+  CUtensorMap tmO[kMaxProblems];    // output stores, 32 x 32 boxes (Gram/Poly: A or B'; Update: X)
+  CUtensorMap tmOT[kMaxProblems];   // transposed-output stores (Gram/Poly: same matrix; Update: X^T)
   GemmProblem prob[kMaxProblems];
   int32_t n_prob;
   int32_t n_tiles;
@@ -101,12 +101,13 @@ struct GemmParams {
 };
 
 // Dynamic shared memory of the GEMM kernel.
+constexpr int kEpiWarps = 8;                                  // two per TMEM lane quarter
 constexpr int kStageBytesA = kBM * kBK * 2;
 constexpr int kStageBytesB = kBN * kBK * 2;
-constexpr int kEpiPitch = 40;                                 // bf16 per transpose row (32 + 8 pad)
-constexpr int kEpiBytesPerWarp = 32 * kEpiPitch * 2;
-constexpr int kGemmSmemBytes =
-    1024 /*align slack*/ + kStages * (kStageBytesA + kStageBytesB) + 4 * kEpiBytesPerWarp + 256 /*barriers*/;
+constexpr int kEpiBlockBytes = 32 * 32 * 2;                   // one dense 32 x 32 bf16 block
+constexpr int kEpiBytesPerWarp = 2 * kEpiBlockBytes;          // direct + transposed staging
+constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageBytesA + kStageBytesB) +
+                               kEpiWarps * kEpiBytesPerWarp + 256 /*barriers*/;
 
 cudaError_t launch_ns_gemm(int phase, const GemmParams& p, int grid, cudaStream_t s);
 int gemm_max_grid();   // SM count of the current device (persistent grid bound)
