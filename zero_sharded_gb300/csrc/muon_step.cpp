@@ -60,6 +60,8 @@ struct Layout {
   int64_t off_status = 0, off_sigma = 0, off_partial = 0, off_momtiles = 0, off_mommats = 0, off_matinfo = 0;
   int64_t off_tiles = 0;           // all GEMM tile lists
   int64_t n_gemm_tiles = 0;
+  int64_t off_cta = 0;             // per launch: grid+1 tile offsets (int32)
+  int64_t n_cta_entries = 0;
   int64_t bytes = 0;
 };
 
@@ -138,6 +140,14 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   }
   L.n_gemm_tiles = nt;
   L.off_tiles = off; off = align_up(off + 16 * std::max<int64_t>(nt, 1), kAlign);
+  // launches per step program: Gram + Poly (one per chunk of kMaxProblems groups),
+  // two Update and two Apply lists (Apply: up to two problems per group)
+  const int64_t G = (int64_t)L.groups.size();
+  const int64_t n_launch = 2 * ceil_div64(std::max<int64_t>(G, 1), kMaxProblems) +
+                           2 * ceil_div64(std::max<int64_t>(G, 1), kMaxProblems) +
+                           2 * ceil_div64(std::max<int64_t>(2 * G, 1), kMaxProblems);
+  L.n_cta_entries = n_launch * (kMaxGrid + 1);
+  L.off_cta = off; off = align_up(off + 4 * L.n_cta_entries, kAlign);
   for (Group& G : L.groups) {
     G.ldx = align_up(G.n, 8);
     G.ldm = align_up(G.m, 8);
@@ -198,7 +208,6 @@ struct Program {
   int64_t tables_begin = 0, tables_end = 0;
   MomParams mom{};
   std::vector<Launch> gram, poly, update[2], apply[2];
-  int grid = 1;
 };
 
 struct Key {
@@ -253,17 +262,40 @@ struct ProbDesc {
   std::vector<int4> tiles;
 };
 
+// Tiles go to CTAs by the LPT rule (Graham): heaviest tile first, each to the
+// currently least-loaded CTA (ties: lower CTA index).  Cost of a tile = its
+// k-blocks plus a constant for the epilogue.  Each CTA's tiles are stored
+// contiguously, heaviest first; cta_first gives the ranges.
+struct TileRef { int4 t; int64_t cost; };
+
 bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int4* host_tiles, int64_t& tile_cursor,
-                   const GemmParams& common, std::vector<Launch>& out, int first, int cur) {
+                   int32_t* dev_cta, int32_t* host_cta, int64_t& cta_cursor, int max_grid, const GemmParams& common,
+                   std::vector<Launch>& out, int first, int cur) {
   for (size_t c0 = 0; c0 < probs.size(); c0 += kMaxProblems) {
     const size_t c1 = std::min(probs.size(), c0 + (size_t)kMaxProblems);
-    std::vector<int4> tl;
-    for (size_t i = c0; i < c1; ++i)
-      for (int4 t : probs[i].tiles) tl.push_back(make_int4((int)(i - c0), t.y, t.z, t.w));
+    std::vector<TileRef> tl;
+    for (size_t i = c0; i < c1; ++i) {
+      const int64_t cost = ceil_div64(probs[i].gp.K, kBK) + 2;
+      for (int4 t : probs[i].tiles) tl.push_back({make_int4((int)(i - c0), t.y, t.z, t.w), cost});
+    }
     if (tl.empty()) continue;
-    std::stable_sort(tl.begin(), tl.end(), [&](const int4& x, const int4& y) {
-      return probs[c0 + x.x].gp.K > probs[c0 + y.x].gp.K;
-    });
+    std::stable_sort(tl.begin(), tl.end(), [](const TileRef& x, const TileRef& y) { return x.cost > y.cost; });
+    const int grid = (int)std::min<int64_t>((int64_t)tl.size(), std::min(max_grid, kMaxGrid));
+    std::vector<std::vector<int4>> per(grid);
+    {
+      // min-heap of (load, cta)
+      std::vector<std::pair<int64_t, int>> heap;
+      for (int b = 0; b < grid; ++b) heap.push_back({0, b});
+      auto gt = [](const std::pair<int64_t, int>& x, const std::pair<int64_t, int>& y) { return x > y; };
+      std::make_heap(heap.begin(), heap.end(), gt);
+      for (const TileRef& r : tl) {
+        std::pop_heap(heap.begin(), heap.end(), gt);
+        auto& top = heap.back();
+        per[top.second].push_back(r.t);
+        top.first += r.cost;
+        std::push_heap(heap.begin(), heap.end(), gt);
+      }
+    }
     Launch ln;
     ln.phase = phase;
     ln.first = first;
@@ -280,9 +312,17 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
     }
     ln.params.first = first;
     ln.params.n_tiles = (int)tl.size();
+    ln.params.grid = grid;
     ln.params.tiles = dev_tiles + tile_cursor;
-    std::copy(tl.begin(), tl.end(), host_tiles + tile_cursor);
+    ln.params.cta_first = dev_cta + cta_cursor;
+    int32_t pos = 0;
+    for (int b = 0; b < grid; ++b) {
+      host_cta[cta_cursor + b] = pos;
+      for (const int4& t : per[b]) host_tiles[tile_cursor + pos++] = t;
+    }
+    host_cta[cta_cursor + grid] = pos;
     tile_cursor += (int64_t)tl.size();
+    cta_cursor += grid + 1;
     out.push_back(ln);
   }
   return true;
@@ -296,7 +336,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   if (st != CZ_OK) return st;
   const int64_t n_mats = (int64_t)L.mats.size();
   P.tables_begin = L.off_sigma;
-  P.tables_end = L.off_tiles + 16 * L.n_gemm_tiles;
+  P.tables_end = L.off_cta + 4 * L.n_cta_entries;
   P.host_tables.assign((size_t)(P.tables_end - P.tables_begin), 0);
   auto& img = P.host_tables;
   const int64_t tb = P.tables_begin;
@@ -371,7 +411,10 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
 
   int4* dev_tiles = reinterpret_cast<int4*>(ws + L.off_tiles);
   int4* host_tiles = at<int4>(img, tb, L.off_tiles);
-  int64_t cursor = 0;
+  int32_t* dev_cta = reinterpret_cast<int32_t*>(ws + L.off_cta);
+  int32_t* host_cta = at<int32_t>(img, tb, L.off_cta);
+  int64_t cursor = 0, cta_cursor = 0;
+  const int max_grid = gemm_max_grid();
   std::vector<ProbDesc> gram, poly, upd[2], app[2];
   for (const Group& G : L.groups) {
     uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x);
@@ -453,15 +496,19 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     }
   }
   // Gram with first=0/1 share one tile list: build first, copy for the other flag.
-  make_launches(kGram, gram, dev_tiles, host_tiles, cursor, common, P.gram, 0, 0);
-  make_launches(kPoly, poly, dev_tiles, host_tiles, cursor, common, P.poly, 0, 0);
+  auto ml = [&](int phase, std::vector<ProbDesc>& probs, std::vector<Launch>& out, int cur) {
+    make_launches(phase, probs, dev_tiles, host_tiles, cursor, dev_cta, host_cta, cta_cursor, max_grid, common, out,
+                  0, cur);
+  };
+  ml(kGram, gram, P.gram, 0);
+  ml(kPoly, poly, P.poly, 0);
   for (int cur = 0; cur < 2; ++cur) {
-    make_launches(kUpdate, upd[cur], dev_tiles, host_tiles, cursor, common, P.update[cur], 0, cur);
-    make_launches(kApply, app[cur], dev_tiles, host_tiles, cursor, common, P.apply[cur], 0, cur);
+    ml(kUpdate, upd[cur], P.update[cur], cur);
+    ml(kApply, app[cur], P.apply[cur], cur);
   }
   (void)ns_steps;
-  if (cursor > L.n_gemm_tiles) return CZ_ERR_NOMEM;   // cannot happen: sized by build_layout
-  P.grid = gemm_max_grid();
+  // cannot happen: both regions are sized by build_layout
+  if (cursor > L.n_gemm_tiles || cta_cursor > L.n_cta_entries) return CZ_ERR_NOMEM;
   return CZ_OK;
 }
 
@@ -616,10 +663,10 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
     for (const Launch& ln : P.gram) {
       gp = ln.params;
       gp.first = first;
-      if (traced(2, s, [&] { return launch_ns_gemm(kGram, gp, P.grid, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+      if (traced(2, s, [&] { return launch_ns_gemm(kGram, gp, gp.grid, s); }) != cudaSuccess) return CZ_ERR_CUDA;
     }
     for (const Launch& ln : P.poly) {
-      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, ln.params, P.grid, s); }) != cudaSuccess)
+      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, ln.params, ln.params.grid, s); }) != cudaSuccess)
         return CZ_ERR_CUDA;
     }
     const bool final_step = t + 1 == ns_steps;
@@ -627,7 +674,7 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
     for (const Launch& ln : last) {
       gp = ln.params;
       gp.first = first;
-      if (traced(final_step ? 5 : 4, s, [&] { return launch_ns_gemm(ln.phase, gp, P.grid, s); }) != cudaSuccess)
+      if (traced(final_step ? 5 : 4, s, [&] { return launch_ns_gemm(ln.phase, gp, gp.grid, s); }) != cudaSuccess)
         return CZ_ERR_CUDA;
     }
   }

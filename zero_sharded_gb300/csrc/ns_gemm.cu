@@ -108,21 +108,31 @@ struct Pre {
 };
 
 template <int PHASE>
-__device__ __forceinline__ void prefetch(Pre& pre, const GemmParams& p, const GemmProblem& pr, int mat, int64_t wrow,
-                                         bool vec_w, int row, bool row_ok, int col0) {
+__device__ __forceinline__ void prefetch(Pre& pre, const GemmParams& p, const GemmProblem& pr, int mat,
+                                         const MatInfo& mi, int rbase, int lane, int col0) {
   if constexpr (PHASE == kPoly) {
+    // A[row][col0 .. col0+31] of this lane's row
+    const int row = rbase + lane;
     const __nv_bfloat16* aux = reinterpret_cast<const __nv_bfloat16*>(pr.aux) + (int64_t)mat * pr.ms_aux +
                                (int64_t)row * pr.ld_aux + col0;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      pre.x[q] = (row_ok && col0 + q * 8 < pr.N) ? *reinterpret_cast<const uint4*>(aux + q * 8)
-                                                  : make_uint4(0u, 0u, 0u, 0u);
+      pre.x[q] = (row < pr.M && col0 + q * 8 < pr.N) ? *reinterpret_cast<const uint4*>(aux + q * 8)
+                                                      : make_uint4(0u, 0u, 0u, 0u);
   }
   if constexpr (PHASE == kApply) {
-    if (row_ok && vec_w && col0 + 32 <= pr.N) {
-      const float4* W = reinterpret_cast<const float4*>(p.W + wrow + col0);
+    // W in the coalesced layout of apply_chunk: entry 4h+i holds row rbase + 8i + lane/4,
+    // columns col0 + 16h + 4(lane%4) .. +3
+    if (mi.vec_ok) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) pre.w[q] = W[q];
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = rbase + i * 8 + (lane >> 2);
+          const int c = col0 + 16 * h + (lane & 3) * 4;
+          if (r < pr.M && c < pr.N)
+            pre.w[4 * h + i] = *reinterpret_cast<const float4*>(p.W + mi.w_off + (int64_t)r * mi.cols + c);
+        }
     }
   }
 }
@@ -140,40 +150,55 @@ __device__ __forceinline__ void stage_block(__nv_bfloat16* D, __nv_bfloat16* T, 
   }
 }
 
-// Apply epilogue of one 32-column chunk: W <- W - lrs * v in the parameter's
-// rows x cols layout, the bf16 copy and the optional debug delta.
-__device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProblem& pr, const MatInfo& mi, int row,
-                                            int col0, float* v, const Pre& pre) {
-  if (row >= pr.M) return;
-  const int64_t wrow = mi.w_off + (int64_t)row * mi.cols;
+// Apply epilogue of one 32-column chunk of the warp's 32 rows.  The fp32 delta
+// lrs * v goes through a padded smem block (lane = row) so that W is read,
+// updated and written with lanes across columns: each instruction touches 8 rows
+// x 64 contiguous bytes instead of 32 rows x 16 bytes.  W was prefetched in the
+// same layout (prefetch<kApply>).  In the parameter's rows x cols layout:
+// W <- W - delta, bf16 copy = RNE(W), optional debug delta.
+constexpr int kApplyPitch = 20;   // floats per staged row (16 + 4): conflict-free v4 writes
+
+__device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProblem& pr, const MatInfo& mi, int rbase,
+                                            int col0, const float* v, const Pre& pre, float* stage, int lane) {
   const float lrs = mi.lrs;
-  if (mi.vec_ok && col0 + 32 <= pr.N) {
-    float4* W = reinterpret_cast<float4*>(p.W + wrow + col0);
+  const bool vec = mi.vec_ok != 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      float4 w = pre.w[q];
-      const float d0 = lrs * v[4 * q], d1 = lrs * v[4 * q + 1], d2 = lrs * v[4 * q + 2], d3 = lrs * v[4 * q + 3];
-      w.x -= d0; w.y -= d1; w.z -= d2; w.w -= d3;
-      W[q] = w;
-      if (p.dbg) reinterpret_cast<float4*>(p.dbg + wrow + col0)[q] = make_float4(d0, d1, d2, d3);
-      v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
-    }
-    if (p.Wb) {
-      uint2* wb = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.Wb) + wrow + col0);
+  for (int h = 0; h < 2; ++h) {
+    __syncwarp();
+    float4* srow = reinterpret_cast<float4*>(stage + lane * kApplyPitch);
 #pragma unroll
-      for (int q = 0; q < 8; ++q)      // 8-byte stores: wrow + col0 is a multiple of 4 elements
-        wb[q] = make_uint2(pack_bf16x2(v[4 * q], v[4 * q + 1]), pack_bf16x2(v[4 * q + 2], v[4 * q + 3]));
-    }
-  } else {
-    float* W = p.W + wrow + col0;
+    for (int q = 0; q < 4; ++q)
+      srow[q] = make_float4(lrs * v[16 * h + 4 * q], lrs * v[16 * h + 4 * q + 1], lrs * v[16 * h + 4 * q + 2],
+                            lrs * v[16 * h + 4 * q + 3]);
+    __syncwarp();
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
-      if (col0 + q < pr.N) {
-        const float d = lrs * v[q];
-        const float w = W[q] - d;
-        W[q] = w;
-        if (p.dbg) p.dbg[wrow + col0 + q] = d;
-        if (p.Wb) reinterpret_cast<__nv_bfloat16*>(p.Wb)[wrow + col0 + q] = __float2bfloat16_rn(w);
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 8 + (lane >> 2);
+      const int c4 = (lane & 3) * 4;
+      const int row = rbase + r;
+      const int col = col0 + 16 * h + c4;
+      if (row >= pr.M || col >= pr.N) continue;
+      const float4 d = *reinterpret_cast<const float4*>(stage + r * kApplyPitch + c4);
+      const int64_t idx = mi.w_off + (int64_t)row * mi.cols + col;
+      if (vec) {   // cols % 4 == 0 and w_off % 4 == 0: the 4 columns are in range and 16-byte aligned
+        float4 w = pre.w[4 * h + i];
+        w.x -= d.x; w.y -= d.y; w.z -= d.z; w.w -= d.w;
+        *reinterpret_cast<float4*>(p.W + idx) = w;
+        if (p.Wb)
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.Wb) + idx) =
+              make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+        if (p.dbg) *reinterpret_cast<float4*>(p.dbg + idx) = d;
+      } else {
+        const float dd[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (col + e < pr.N) {
+            const float w = p.W[idx + e] - dd[e];
+            p.W[idx + e] = w;
+            if (p.Wb) reinterpret_cast<__nv_bfloat16*>(p.Wb)[idx + e] = __float2bfloat16_rn(w);
+            if (p.dbg) p.dbg[idx + e] = dd[e];
+          }
+        }
       }
     }
   }
@@ -206,6 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_holder;
+  // this CTA's tiles (host LPT assignment, heaviest first)
+  const int t_begin = p.cta_first[blockIdx.x];
+  const int t_end = p.cta_first[blockIdx.x + 1];
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -221,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;   // bit s: parity of stage s's last fill
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+    for (int t = t_begin; t < t_end && ok; ++t) {
       const int4 tl = p.tiles[t];
       const int nk = ceil_div(p.prob[tl.x].K, kBK);
       const CUtensorMap* ma = &p.tmA[tl.x];
@@ -259,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+    for (int t = t_begin; t < t_end && ok; ++t) {
       const int4 tl = p.tiles[t];
       const int nk = ceil_div(p.prob[tl.x].K, kBK);
       bool w = true;
@@ -317,14 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     const uint32_t lane_field = (uint32_t)(quad * 32) << 16;
     uint32_t acc = 0, acc_phase = 0;
     bool pending = false;                       // bulk stores in flight from the staging blocks
-    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+    for (int t = t_begin; t < t_end; ++t) {
       const int4 tl = p.tiles[t];
       const GemmProblem& pr = p.prob[tl.x];
       const int mat = tl.y;
       const int gm = pr.mat_base + mat;
       const int rbase = tl.z * kBM + quad * 32;
-      const int row = rbase + lane;
-      const bool row_ok = row < pr.M;
       const int ch_first = half * 4;
       const int col_first = tl.w * kBN + ch_first * 32;
       // chunks this warp reads from TMEM (warp-uniform bit mask)
@@ -343,14 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         s = (PHASE == kGram) ? sg * sg : sg;
       }
       MatInfo mi{};
-      int64_t wrow = 0;
-      if constexpr (PHASE == kApply) {
-        mi = p.mats[gm];
-        wrow = mi.w_off + (int64_t)row * mi.cols;
-      }
+      if constexpr (PHASE == kApply) mi = p.mats[gm];
       Pre cur;
       const int first_c = need ? __ffs(need) - 1 : 0;
-      if (need) prefetch<PHASE>(cur, p, pr, mat, wrow, mi.vec_ok != 0, row, row_ok, col_first + first_c * 32);
+      if (need) prefetch<PHASE>(cur, p, pr, mat, mi, rbase, lane, col_first + first_c * 32);
       const bool w = mbar_wait(&sm.tfull[acc], acc_phase, abort, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, w)) break;
       tc_fence_after();
@@ -364,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         const int col0 = col_first + c * 32;
         Pre nxt;
         const uint32_t later = need >> (c + 1);
-        if (later) prefetch<PHASE>(nxt, p, pr, mat, wrow, mi.vec_ok != 0, row, row_ok, col0 + 32 * __ffs(later));
+        if (later) prefetch<PHASE>(nxt, p, pr, mat, mi, rbase, lane, col0 + 32 * __ffs(later));
         float v[32];
         tmem_ld32(tbase + (uint32_t)((ch_first + c) * 32), v);
         if (c == last) {                 // accumulator no longer needed: let the MMA reuse it
@@ -374,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         if constexpr (PHASE == kApply) {
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] *= s;
-          apply_chunk(p, pr, mi, row, col0, v, cur);
+          apply_chunk(p, pr, mi, rbase, col0, v, cur, reinterpret_cast<float*>(stD), lane);
         } else {
           if constexpr (PHASE == kPoly) {
             // B' = a I + b A + c (A A)
@@ -437,7 +459,8 @@ cudaError_t launch_phase(const GemmParams& p, int grid, cudaStream_t s) {
 
 cudaError_t launch_ns_gemm(int phase, const GemmParams& p, int grid, cudaStream_t s) {
   if (p.n_tiles <= 0) return cudaSuccess;
-  if (grid > p.n_tiles) grid = p.n_tiles;
+  (void)grid;
+  grid = p.grid;
   switch (phase) {
     case kGram: return launch_phase<kGram>(p, grid, s);
     case kPoly: return launch_phase<kPoly>(p, grid, s);

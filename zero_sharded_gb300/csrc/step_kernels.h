@@ -53,6 +53,7 @@ constexpr int kBN = 256;        // UMMA N (TMEM columns per accumulator)
 constexpr int kBK = 64;         // 64 bf16 = one 128-byte swizzle row
 constexpr int kStages = 4;
 constexpr int kMaxProblems = 16;
+constexpr int kMaxGrid = 1024;  // upper bound on the persistent grid (SM count)
 
 enum Phase : int32_t {
   kGram = 0,     // A = s^2 X X^T                   (symmetric output)
@@ -88,7 +89,9 @@ struct GemmParams {
   GemmProblem prob[kMaxProblems];
   int32_t n_prob;
   int32_t n_tiles;
-  const int4* tiles;      // {problem, matrix, tile_m, tile_n}
+  int32_t grid;           // CTAs the tile assignment was made for
+  const int4* tiles;      // {problem, matrix, tile_m, tile_n}, grouped by CTA
+  const int32_t* cta_first;   // grid+1 entries: CTA b runs tiles [cta_first[b], cta_first[b+1])
   const float* sigma;     // per global matrix
   const MatInfo* mats;    // per global matrix
   float a, b, c;
