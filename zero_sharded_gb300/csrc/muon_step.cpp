@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <memory>
@@ -162,6 +163,16 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   return CZ_OK;
 }
 
+// Newton-Schulz GEMM variant: CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles)
+// by default; CZ_NS_PAIR=0 selects single-CTA 128 x 256 tiles.
+bool use_pair() {
+  static const bool pair = [] {
+    const char* e = std::getenv("CZ_NS_PAIR");
+    return !(e && e[0] == '0');
+  }();
+  return pair;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -203,6 +214,7 @@ struct Launch {
 // Everything that depends only on (plan, rank, shapes, offsets, buffers, options).
 struct Program {
   uint64_t uid = next_uid();
+  bool pair = true;
   Layout L;
   std::vector<uint8_t> host_tables;   // image of [off_sigma .. off_tiles + tiles) region (tables only)
   int64_t tables_begin = 0, tables_end = 0;
@@ -414,7 +426,10 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   int32_t* dev_cta = reinterpret_cast<int32_t*>(ws + L.off_cta);
   int32_t* host_cta = at<int32_t>(img, tb, L.off_cta);
   int64_t cursor = 0, cta_cursor = 0;
-  const int max_grid = gemm_max_grid();
+  const bool pair = P.pair = use_pair();
+  const int tm_rows = pair ? 256 : kBM;          // output rows per tile
+  const uint32_t b_box = pair ? 128 : kBN;       // B-side rows each CTA loads per stage
+  const int max_grid = gemm_max_units(pair);
   std::vector<ProbDesc> gram, poly, upd[2], app[2];
   for (const Group& G : L.groups) {
     uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x);
@@ -426,14 +441,14 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     // symmetric tiles of an m x m output
     std::vector<int4> sym;
     for (int j = 0; j < c; ++j)
-      for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
+      for (int64_t a = 0; a < ceil_div64(G.m, tm_rows); ++a)
         for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b)
-          if (a * kBM <= b * kBN + kBN - 1) sym.push_back(make_int4(0, j, (int)a, (int)b));
+          if (a * tm_rows <= b * kBN + kBN - 1) sym.push_back(make_int4(0, j, (int)a, (int)b));
     {
       // Gram: A = s^2 X X^T, stored with its mirror into A
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.n; d.gp.count = c; d.gp.mat_base = G.mat_base;
-      if (!encode_map(&d.ta, X, G.n, G.m, c, G.ldx, msx, kBM) || !encode_map(&d.tb, X, G.n, G.m, c, G.ldx, msx, kBN) ||
+      if (!encode_map(&d.ta, X, G.n, G.m, c, G.ldx, msx, kBM) || !encode_map(&d.tb, X, G.n, G.m, c, G.ldx, msx, b_box) ||
           !encode_map(&d.to, A, G.m, G.m, c, G.ldm, msa, 0, true))
         return CZ_ERR_CUDA;
       d.tot = d.to;
@@ -445,7 +460,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
       d.gp.aux = A; d.gp.ld_aux = G.ldm; d.gp.ms_aux = msa;
-      if (!encode_map(&d.ta, A, G.m, G.m, c, G.ldm, msa, kBM) || !encode_map(&d.tb, A, G.m, G.m, c, G.ldm, msa, kBN) ||
+      if (!encode_map(&d.ta, A, G.m, G.m, c, G.ldm, msa, kBM) || !encode_map(&d.tb, A, G.m, G.m, c, G.ldm, msa, b_box) ||
           !encode_map(&d.to, B, G.m, G.m, c, G.ldm, msa, 0, true))
         return CZ_ERR_CUDA;
       d.tot = d.to;
@@ -458,12 +473,12 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.n; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
       if (!encode_map(&d.ta, B, G.m, G.m, c, G.ldm, msa, kBM) ||
-          !encode_map(&d.tb, XT[cur], G.m, G.n, c, G.ldm, mst, kBN) ||
+          !encode_map(&d.tb, XT[cur], G.m, G.n, c, G.ldm, mst, b_box) ||
           !encode_map(&d.to, X, G.n, G.m, c, G.ldx, msx, 0, true) ||
           !encode_map(&d.tot, XT[cur ^ 1], G.m, G.n, c, G.ldm, mst, 0, true))
         return CZ_ERR_CUDA;
       for (int j = 0; j < c; ++j)
-        for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
+        for (int64_t a = 0; a < ceil_div64(G.m, tm_rows); ++a)
           for (int64_t b = 0; b < ceil_div64(G.n, kBN); ++b) d.tiles.push_back(make_int4(0, j, (int)a, (int)b));
       upd[cur].push_back(d);
       // apply, wide tensors: output X (m x n) = parameter layout
@@ -473,7 +488,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         e.tiles.clear();
         for (int j = 0; j < c; ++j) {
           if (L.mats[G.mat_base + j].tall) continue;
-          for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
+          for (int64_t a = 0; a < ceil_div64(G.m, tm_rows); ++a)
             for (int64_t b = 0; b < ceil_div64(G.n, kBN); ++b) e.tiles.push_back(make_int4(0, j, (int)a, (int)b));
         }
         app[cur].push_back(e);
@@ -484,11 +499,11 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         e.gp.M = G.n; e.gp.N = G.m; e.gp.K = G.m; e.gp.count = c; e.gp.mat_base = G.mat_base;
         e.gp.orient = 1;
         if (!encode_map(&e.ta, XT[cur], G.m, G.n, c, G.ldm, mst, kBM) ||
-            !encode_map(&e.tb, B, G.m, G.m, c, G.ldm, msa, kBN))
+            !encode_map(&e.tb, B, G.m, G.m, c, G.ldm, msa, b_box))
           return CZ_ERR_CUDA;
         for (int j = 0; j < c; ++j) {
           if (!L.mats[G.mat_base + j].tall) continue;
-          for (int64_t a = 0; a < ceil_div64(G.n, kBM); ++a)
+          for (int64_t a = 0; a < ceil_div64(G.n, tm_rows); ++a)
             for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b) e.tiles.push_back(make_int4(0, j, (int)a, (int)b));
         }
         app[cur].push_back(e);
@@ -663,10 +678,10 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
     for (const Launch& ln : P.gram) {
       gp = ln.params;
       gp.first = first;
-      if (traced(2, s, [&] { return launch_ns_gemm(kGram, gp, gp.grid, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+      if (traced(2, s, [&] { return launch_ns_gemm(kGram, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
     }
     for (const Launch& ln : P.poly) {
-      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, ln.params, ln.params.grid, s); }) != cudaSuccess)
+      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, P.pair, ln.params, s); }) != cudaSuccess)
         return CZ_ERR_CUDA;
     }
     const bool final_step = t + 1 == ns_steps;
@@ -674,7 +689,7 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
     for (const Launch& ln : last) {
       gp = ln.params;
       gp.first = first;
-      if (traced(final_step ? 5 : 4, s, [&] { return launch_ns_gemm(ln.phase, gp, gp.grid, s); }) != cudaSuccess)
+      if (traced(final_step ? 5 : 4, s, [&] { return launch_ns_gemm(ln.phase, P.pair, gp, s); }) != cudaSuccess)
         return CZ_ERR_CUDA;
     }
   }

@@ -44,9 +44,24 @@ namespace {
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 
+// Geometry of the two variants: one CTA per 128 x 256 tile, or a CTA pair per
+// 256 x 256 tile (cta_group::2: each CTA holds 128 rows of A and 128 of the 256
+// B rows per stage, and receives its 128 x 256 half of the accumulator).
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kTileM = PAIR ? 256 : 128;
+  static constexpr int kRowsB = PAIR ? 128 : 256;
+  static constexpr int kBytesA = 128 * kBK * 2;
+  static constexpr int kBytesB = kRowsB * kBK * 2;
+  static constexpr int kStageBytes = kBytesA + kBytesB;
+};
+static_assert(Cfg<true>::kStages * Cfg<true>::kStageBytes <= kStages * (kStageBytesA + kStageBytesB), "smem");
+static_assert(Cfg<false>::kStages * Cfg<false>::kStageBytes <= kStages * (kStageBytesA + kStageBytesB), "smem");
+
 struct Smem {
-  uint8_t* a;              // kStages A tiles of kStageBytesA (1024-byte aligned)
-  uint8_t* b;              // kStages B tiles of kStageBytesB
+  uint8_t* a;              // kStages A tiles (1024-byte aligned)
+  uint8_t* b;              // kStages B tiles
   __nv_bfloat16* epi;      // kEpiWarps x (direct + transposed 32 x 32 bf16 staging blocks)
   uint64_t* full;          // [kStages]
   uint64_t* empty;         // [kStages]
@@ -57,24 +72,26 @@ struct Smem {
   int* abort;
 };
 
+template <bool PAIR>
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
+  using C = Cfg<PAIR>;
   Smem s;
   const uint32_t base = smem_u32(raw);
   uint8_t* p = raw + ((1024u - (base & 1023u)) & 1023u);
   s.a = p;
-  p += kStages * kStageBytesA;
+  p += C::kStages * C::kBytesA;
   s.b = p;
-  p += kStages * kStageBytesB;
+  p += C::kStages * C::kBytesB;
   s.epi = reinterpret_cast<__nv_bfloat16*>(p);
   p += kEpiWarps * kEpiBytesPerWarp;
   uint64_t* bars = reinterpret_cast<uint64_t*>(p);
   s.full = bars;
-  s.empty = bars + kStages;
-  s.tfull = bars + 2 * kStages;
-  s.tempty = bars + 2 * kStages + 2;
-  s.drain = bars + 2 * kStages + 4;
-  s.tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
-  s.abort = reinterpret_cast<int*>(bars + 2 * kStages + 6);
+  s.empty = bars + C::kStages;
+  s.tfull = bars + 2 * C::kStages;
+  s.tempty = bars + 2 * C::kStages + 2;
+  s.drain = bars + 2 * C::kStages + 4;
+  s.tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 5);
+  s.abort = reinterpret_cast<int*>(bars + 2 * C::kStages + 6);
   return s;
 }
 
@@ -204,39 +221,46 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProbl
   }
 }
 
-template <int PHASE>
+template <int PHASE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
-  Smem sm = carve(smem_raw);
+  Smem sm = carve<PAIR>(smem_raw);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort = sm.abort;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;     // 0: the CTA that issues the MMAs
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tfull[i], 1);
-      mbar_init(&sm.tempty[i], 32 * kEpiWarps);
+      mbar_init(&sm.tempty[i], kEpiWarps * (PAIR ? 2 : 1));   // one arrival per epilogue warp
     }
     mbar_init(sm.drain, 1);
     *sm.abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) tmem_alloc(sm.tmem_holder, kTmemCols);
+  if (warp == 1) {
+    if constexpr (PAIR) tmem_alloc_pair(sm.tmem_holder, kTmemCols);
+    else tmem_alloc(sm.tmem_holder, kTmemCols);
+  }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // the peer's barriers exist before any remote arrival
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_holder;
-  // this CTA's tiles (host LPT assignment, heaviest first)
-  const int t_begin = p.cta_first[blockIdx.x];
-  const int t_end = p.cta_first[blockIdx.x + 1];
+  // this unit's tiles (host LPT assignment, heaviest first)
+  const int t_begin = p.cta_first[unit];
+  const int t_end = p.cta_first[unit + 1];
 
   if (warp == 0) {
-    // ---------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------- TMA producer (both CTAs of a pair)
     if (lane == 0) {
       for (int i = 0; i < p.n_prob; ++i) {
         tma_prefetch_desc(&p.tmA[i]);
@@ -254,14 +278,26 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       const int nk = ceil_div(p.prob[tl.x].K, kBK);
       const CUtensorMap* ma = &p.tmA[tl.x];
       const CUtensorMap* mb = &p.tmB[tl.x];
+      const int arow = tl.z * C::kTileM + (int)rank * 128;
+      const int brow = tl.w * kBN + (int)rank * C::kRowsB;
       for (int kb = 0; kb < nk; ++kb) {
         bool w = true;
         if (lane == 0) {
           w = mbar_wait(&sm.empty[stage], phase ^ 1u, abort, p.status, p.timeout_ns);
           if (w) {
-            mbar_arrive_expect_tx(&sm.full[stage], kStageBytesA + kStageBytesB);
-            tma_load_3d(sm.a + stage * kStageBytesA, ma, &sm.full[stage], kb * kBK, tl.z * kBM, tl.y);
-            tma_load_3d(sm.b + stage * kStageBytesB, mb, &sm.full[stage], kb * kBK, tl.w * kBN, tl.y);
+            uint8_t* da = sm.a + stage * C::kBytesA;
+            uint8_t* db = sm.b + stage * C::kBytesB;
+            if constexpr (PAIR) {
+              // both CTAs' copies complete on the even CTA's full barrier
+              const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), 0);
+              if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * C::kStageBytes);
+              tma_load_3d_pair(da, ma, fb, kb * kBK, arow, tl.y);
+              tma_load_3d_pair(db, mb, fb, kb * kBK, brow, tl.y);
+            } else {
+              mbar_arrive_expect_tx(&sm.full[stage], C::kStageBytes);
+              tma_load_3d(da, ma, &sm.full[stage], kb * kBK, arow, tl.y);
+              tma_load_3d(db, mb, &sm.full[stage], kb * kBK, brow, tl.y);
+            }
             issued |= 1u << stage;
             last_par = (last_par & ~(1u << stage)) | (phase << stage);
           }
@@ -270,68 +306,78 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           ok = false;
           break;
         }
-        if (++stage == kStages) {
+        if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // every issued copy must land before the CTA may exit
-    if (lane == 0) {
-      for (int s = 0; s < kStages; ++s)
+    // every issued copy must land before the CTA may exit; a pair's copies are
+    // counted on the even CTA's barriers, and the odd CTA waits for the even one
+    // at the final cluster barrier
+    if (lane == 0 && rank == 0) {
+      for (int s = 0; s < C::kStages; ++s)
         if (issued & (1u << s)) mbar_wait(&sm.full[s], (last_par >> s) & 1u, nullptr, p.status, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
-    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-    bool ok = true;
-    for (int t = t_begin; t < t_end && ok; ++t) {
-      const int4 tl = p.tiles[t];
-      const int nk = ceil_div(p.prob[tl.x].K, kBK);
-      bool w = true;
-      if (lane == 0) w = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort, p.status, p.timeout_ns);
-      if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
-      tc_fence_after();
-      const uint32_t d = tmem_base + acc * (uint32_t)kBN;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (lane == 0) w = mbar_wait(&sm.full[stage], phase, abort, p.status, p.timeout_ns);
-        if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
-          ok = false;
-          break;
-        }
+    // ---------------------------------------------------------- MMA issuer (even CTA only)
+    if (rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(C::kTileM, kBN);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        const int4 tl = p.tiles[t];
+        const int nk = ceil_div(p.prob[tl.x].K, kBK);
+        bool w = true;
+        if (lane == 0) w = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort, p.status, p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = smem_u32(sm.a + stage * kStageBytesA);
-          const uint32_t b0 = smem_u32(sm.b + stage * kStageBytesB);
-#pragma unroll
-          for (int s = 0; s < kBK / 16; ++s) {
-            umma_bf16(d, sdesc_kmajor_sw128(a0 + s * 32), sdesc_kmajor_sw128(b0 + s * 32), idesc,
-                      (kb | s) != 0 ? 1u : 0u);
+        const uint32_t d = tmem_base + acc * (uint32_t)kBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (lane == 0) w = mbar_wait(&sm.full[stage], phase, abort, p.status, p.timeout_ns);
+          if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+            ok = false;
+            break;
           }
-          umma_commit(&sm.empty[stage]);
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = smem_u32(sm.a + stage * C::kBytesA);
+            const uint32_t b0 = smem_u32(sm.b + stage * C::kBytesB);
+#pragma unroll
+            for (int s = 0; s < kBK / 16; ++s) {
+              const uint64_t ad = sdesc_kmajor_sw128(a0 + s * 32), bd = sdesc_kmajor_sw128(b0 + s * 32);
+              if constexpr (PAIR) umma_bf16_pair(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+              else umma_bf16(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+            }
+            if constexpr (PAIR) umma_commit_pair(&sm.empty[stage], 0x3);   // frees the stage in both CTAs
+            else umma_commit(&sm.empty[stage]);
+          }
+          __syncwarp();
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if constexpr (PAIR) umma_commit_pair(&sm.tfull[acc], 0x3);     // both halves of the accumulator
+          else umma_commit(&sm.tfull[acc]);
         }
         __syncwarp();
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok) break;
-      if (lane == 0) umma_commit(&sm.tfull[acc]);
+      // wait until every issued MMA has completed (TMEM is released below)
+      if (lane == 0) {
+        if constexpr (PAIR) umma_commit_pair(sm.drain, 0x1);
+        else umma_commit(sm.drain);
+        mbar_wait(sm.drain, 0, nullptr, p.status, p.timeout_ns);
+      }
       __syncwarp();
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
     }
-    // wait until every issued MMA has completed (TMEM is released below)
-    if (lane == 0) {
-      umma_commit(sm.drain);
-      mbar_wait(sm.drain, 0, nullptr, p.status, p.timeout_ns);
-    }
-    __syncwarp();
   } else {
-    // ---------------------------------------------------------- epilogue
+    // ---------------------------------------------------------- epilogue (both CTAs of a pair)
     // Symmetric outputs (Gram, Poly) are written by aligned 32 x 32 blocks: a
     // block above the diagonal is stored directly and mirrored, a diagonal block
     // directly only, a block below the diagonal not at all (its mirror comes from
@@ -345,12 +391,21 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     const uint32_t lane_field = (uint32_t)(quad * 32) << 16;
     uint32_t acc = 0, acc_phase = 0;
     bool pending = false;                       // bulk stores in flight from the staging blocks
+    // the accumulator buffer is handed back to the MMA issuer (even CTA) once per warp
+    auto release = [&](uint32_t buf) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.tempty[buf]), 0));
+        else mbar_arrive(&sm.tempty[buf]);
+      }
+    };
     for (int t = t_begin; t < t_end; ++t) {
       const int4 tl = p.tiles[t];
       const GemmProblem& pr = p.prob[tl.x];
       const int mat = tl.y;
       const int gm = pr.mat_base + mat;
-      const int rbase = tl.z * kBM + quad * 32;
+      const int rbase = tl.z * C::kTileM + (int)rank * 128 + quad * 32;
       const int ch_first = half * 4;
       const int col_first = tl.w * kBN + ch_first * 32;
       // chunks this warp reads from TMEM (warp-uniform bit mask)
@@ -377,10 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       if (!__all_sync(0xffffffffu, w)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + acc * (uint32_t)kBN + lane_field;
-      if (last < 0) {
-        tc_fence_before();
-        mbar_arrive(&sm.tempty[acc]);
-      }
+      if (last < 0) release(acc);
       for (int c = first_c; c <= last; ++c) {
         if (!((need >> c) & 1u)) continue;
         const int col0 = col_first + c * 32;
@@ -389,10 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         if (later) prefetch<PHASE>(nxt, p, pr, mat, mi, rbase, lane, col0 + 32 * __ffs(later));
         float v[32];
         tmem_ld32(tbase + (uint32_t)((ch_first + c) * 32), v);
-        if (c == last) {                 // accumulator no longer needed: let the MMA reuse it
-          tc_fence_before();
-          mbar_arrive(&sm.tempty[acc]);
-        }
+        if (c == last) release(acc);     // accumulator no longer needed: let the MMA reuse it
         if constexpr (PHASE == kApply) {
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] *= s;
@@ -433,48 +482,90 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // the even CTA's MMAs (which read both CTAs' smem) are done
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <int PHASE>
-cudaError_t launch_phase(const GemmParams& p, int grid, cudaStream_t s) {
+template <int PHASE, bool PAIR>
+cudaError_t launch_phase(const GemmParams& p, cudaStream_t s) {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(ns_gemm_kernel<PHASE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    e = cudaFuncSetAttribute(ns_gemm_kernel<PHASE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kGemmSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  ns_gemm_kernel<PHASE><<<grid, kThreads, kGemmSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * p.grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<PHASE, PAIR>, p);
+  } else {
+    ns_gemm_kernel<PHASE, PAIR><<<p.grid, kThreads, kGemmSmemBytes, s>>>(p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_ns_gemm(int phase, const GemmParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_ns_gemm(int phase, bool pair, const GemmParams& p, cudaStream_t s) {
   if (p.n_tiles <= 0) return cudaSuccess;
-  (void)grid;
-  grid = p.grid;
-  switch (phase) {
-    case kGram: return launch_phase<kGram>(p, grid, s);
-    case kPoly: return launch_phase<kPoly>(p, grid, s);
-    case kUpdate: return launch_phase<kUpdate>(p, grid, s);
-    case kApply: return launch_phase<kApply>(p, grid, s);
+  switch (phase * 2 + (pair ? 1 : 0)) {
+    case kGram * 2: return launch_phase<kGram, false>(p, s);
+    case kGram * 2 + 1: return launch_phase<kGram, true>(p, s);
+    case kPoly * 2: return launch_phase<kPoly, false>(p, s);
+    case kPoly * 2 + 1: return launch_phase<kPoly, true>(p, s);
+    case kUpdate * 2: return launch_phase<kUpdate, false>(p, s);
+    case kUpdate * 2 + 1: return launch_phase<kUpdate, true>(p, s);
+    case kApply * 2: return launch_phase<kApply, false>(p, s);
+    case kApply * 2 + 1: return launch_phase<kApply, true>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-int gemm_max_grid() {
+int gemm_max_units(bool pair) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
-  return sms > 0 ? sms : 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) return 1;
+  if (!pair) return sms;
+  // CTA pairs that can be resident at once (clusters of 2 need two SMs of one GPC)
+  if (cudaFuncSetAttribute(ns_gemm_kernel<kUpdate, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kGemmSmemBytes) != cudaSuccess)
+    return sms / 2 > 0 ? sms / 2 : 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, ns_gemm_kernel<kUpdate, true>, &cfg) != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    return sms / 2 > 0 ? sms / 2 : 1;
+  }
+  return clusters;
 }
 
 }  // namespace cz

@@ -89,9 +89,9 @@ struct GemmParams {
   GemmProblem prob[kMaxProblems];
   int32_t n_prob;
   int32_t n_tiles;
-  int32_t grid;           // CTAs the tile assignment was made for
+  int32_t grid;           // units (CTAs, or CTA pairs) the tile assignment was made for
   const int4* tiles;      // {problem, matrix, tile_m, tile_n}, grouped by CTA
-  const int32_t* cta_first;   // grid+1 entries: CTA b runs tiles [cta_first[b], cta_first[b+1])
+  const int32_t* cta_first;   // grid+1 entries: unit b runs tiles [cta_first[b], cta_first[b+1])
   const float* sigma;     // per global matrix
   const MatInfo* mats;    // per global matrix
   float a, b, c;
@@ -112,7 +112,9 @@ constexpr int kEpiBytesPerWarp = 2 * kEpiBlockBytes;          // direct + transp
 constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageBytesA + kStageBytesB) +
                                kEpiWarps * kEpiBytesPerWarp + 256 /*barriers*/;
 
-cudaError_t launch_ns_gemm(int phase, const GemmParams& p, int grid, cudaStream_t s);
-int gemm_max_grid();   // SM count of the current device (persistent grid bound)
+// pair: 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2), else 128 x 256 tiles
+// on single CTAs.  p.grid counts units (pairs or CTAs).
+cudaError_t launch_ns_gemm(int phase, bool pair, const GemmParams& p, cudaStream_t s);
+int gemm_max_units(bool pair);   // units that can be resident at once (persistent grid bound)
 
 }  // namespace cz
