@@ -280,6 +280,25 @@ struct ProbDesc {
 // contiguously, heaviest first; cta_first gives the ranges.
 struct TileRef { int4 t; int64_t cost; };
 
+// Tiles of one matrix in an L2-friendly order.  Consecutive list entries run at
+// the same time (one per unit), so the list walks the larger operand in groups of
+// `group` row blocks while sweeping the smaller operand fully inside each group:
+// the group's large blocks plus the whole small operand stay in L2, and each large
+// block is read from HBM once instead of once per row of tiles.
+// big_is_n: the B side (tile_n index) is the large operand.
+void grouped_tiles(std::vector<int4>& out, int mat, int64_t TM, int64_t TN, bool big_is_n, int64_t group) {
+  if (group < 1) group = 1;
+  if (big_is_n) {
+    for (int64_t b0 = 0; b0 < TN; b0 += group)
+      for (int64_t a = 0; a < TM; ++a)
+        for (int64_t b = b0; b < std::min(TN, b0 + group); ++b) out.push_back(make_int4(0, mat, (int)a, (int)b));
+  } else {
+    for (int64_t a0 = 0; a0 < TM; a0 += group)
+      for (int64_t b = 0; b < TN; ++b)
+        for (int64_t a = a0; a < std::min(TM, a0 + group); ++a) out.push_back(make_int4(0, mat, (int)a, (int)b));
+  }
+}
+
 bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int4* host_tiles, int64_t& tile_cursor,
                    int32_t* dev_cta, int32_t* host_cta, int64_t& cta_cursor, int max_grid, const GemmParams& common,
                    std::vector<Launch>& out, int first, int cur) {
@@ -477,9 +496,10 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
           !encode_map(&d.to, X, G.n, G.m, c, G.ldx, msx, 0, true) ||
           !encode_map(&d.tot, XT[cur ^ 1], G.m, G.n, c, G.ldm, mst, 0, true))
         return CZ_ERR_CUDA;
-      for (int j = 0; j < c; ++j)
-        for (int64_t a = 0; a < ceil_div64(G.m, tm_rows); ++a)
-          for (int64_t b = 0; b < ceil_div64(G.n, kBN); ++b) d.tiles.push_back(make_int4(0, j, (int)a, (int)b));
+      // update tiles: B' (m x m) is the small operand, X^T (n x m) the large one
+      const int64_t TMu = ceil_div64(G.m, tm_rows), TNu = ceil_div64(G.n, kBN);
+      const int64_t grp_u = ceil_div64(max_grid, TMu);
+      for (int j = 0; j < c; ++j) grouped_tiles(d.tiles, j, TMu, TNu, true, grp_u);
       upd[cur].push_back(d);
       // apply, wide tensors: output X (m x n) = parameter layout
       if (G.has_wide) {
@@ -488,8 +508,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         e.tiles.clear();
         for (int j = 0; j < c; ++j) {
           if (L.mats[G.mat_base + j].tall) continue;
-          for (int64_t a = 0; a < ceil_div64(G.m, tm_rows); ++a)
-            for (int64_t b = 0; b < ceil_div64(G.n, kBN); ++b) e.tiles.push_back(make_int4(0, j, (int)a, (int)b));
+          grouped_tiles(e.tiles, j, TMu, TNu, true, grp_u);
         }
         app[cur].push_back(e);
       }
@@ -501,10 +520,12 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         if (!encode_map(&e.ta, XT[cur], G.m, G.n, c, G.ldm, mst, kBM) ||
             !encode_map(&e.tb, B, G.m, G.m, c, G.ldm, msa, b_box))
           return CZ_ERR_CUDA;
+        // X^T (n x m, A side) is the large operand, B' (m x m, B side) the small one
+        const int64_t TMt = ceil_div64(G.n, tm_rows), TNt = ceil_div64(G.m, kBN);
+        const int64_t grp_t = ceil_div64(max_grid, TNt);
         for (int j = 0; j < c; ++j) {
           if (!L.mats[G.mat_base + j].tall) continue;
-          for (int64_t a = 0; a < ceil_div64(G.n, tm_rows); ++a)
-            for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b) e.tiles.push_back(make_int4(0, j, (int)a, (int)b));
+          grouped_tiles(e.tiles, j, TMt, TNt, false, grp_t);
         }
         app[cur].push_back(e);
       }
