@@ -105,8 +105,11 @@ def build_workload(name: str, world: int, rank: int):
         buckets = cz.cz_make_buckets(w.numels, BUCKET_CAP) if world > 1 else [len(w.numels)]
         return w, buckets, world, 1.0, rank
     if name == "tiny":
-        w = wl.tiny()
-        return w, [len(w.numels)], 1, 1.0, 0
+        # one copy of the six tiny matrices per rank, one bucket per copy, planned with R = world
+        base = wl.tiny()
+        w = wl.Workload("tiny-6" if world == 1 else f"tiny-6x{world}", base.shapes * world,
+                        [f"r{k}.{n}" for k in range(world) for n in base.names], base.param_std, base.grad_std)
+        return w, [len(base.shapes)] * world, world, 1.0, rank
     if name == "qwen3-1.7b-28L":
         w = wl.qwen3_1p7b_layers(28)
         return w, [len(w.numels)], 1, 1.0, 0

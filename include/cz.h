@@ -188,6 +188,15 @@ int cz_device_status(void* stream, void* workspace, int* status_out);
 int cz_profile_enable(int32_t on);
 int cz_profile_read(double* ms, int64_t* launches, int32_t n_kinds);
 
+/* Self-test of the device-side failure detection (support; no counterpart in
+ * the paper).  Launches one CTA on `stream` that waits, with the same bounded
+ * wait the step's kernels use, on an mbarrier that nothing ever completes; after
+ * timeout_ns (0 .. 2e9) the wait gives up and records CZ_ERR_TIMEOUT in the
+ * status word of `workspace` (a device buffer of >= 256 bytes whose first int
+ * starts at zero), which cz_device_status then reports.  No fault, no trap: the
+ * context stays usable.  Returns CZ_OK when enqueued. */
+int cz_selftest_bounded_wait(int64_t timeout_ns, void* workspace, void* stream);
+
 /* Static string for a status code. */
 const char* cz_status_string(int status);
 

@@ -42,6 +42,9 @@ namespace cz {
 namespace {
 
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Limit of the drain waits at exit (in-flight TMA copies and MMAs must finish
+// before shared memory and TMEM are released); independent of p.timeout_ns.
+constexpr int64_t kDrainTimeoutNs = 2000000000LL;
 constexpr uint32_t kTmemCols = 512;
 
 // Geometry of the two variants: one CTA per 128 x 256 tile, or a CTA pair per
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     // at the final cluster barrier
     if (lane == 0 && rank == 0) {
       for (int s = 0; s < C::kStages; ++s)
-        if (issued & (1u << s)) mbar_wait(&sm.full[s], (last_par >> s) & 1u, nullptr, p.status, p.timeout_ns);
+        if (issued & (1u << s)) mbar_wait(&sm.full[s], (last_par >> s) & 1u, nullptr, p.status, kDrainTimeoutNs);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -372,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       if (lane == 0) {
         if constexpr (PAIR) umma_commit_pair(sm.drain, 0x1);
         else umma_commit(sm.drain);
-        mbar_wait(sm.drain, 0, nullptr, p.status, p.timeout_ns);
+        mbar_wait(sm.drain, 0, nullptr, p.status, kDrainTimeoutNs);
       }
       __syncwarp();
     }

@@ -92,6 +92,7 @@ def load() -> ctypes.CDLL:
         "cz_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, _i32p]),
         "cz_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
         "cz_profile_read": (ctypes.c_int, [_f64p, _i64p, ctypes.c_int32]),
+        "cz_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
         "cz_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "cz_version": (ctypes.c_char_p, []),
     }
@@ -302,3 +303,8 @@ def cz_profile_read() -> dict:
     cnt = (ctypes.c_int64 * n)()
     _check("cz_profile_read", load().cz_profile_read(ms, cnt, n))
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def cz_selftest_bounded_wait(timeout_ns: int, workspace, stream=None) -> None:
+    _check("cz_selftest_bounded_wait", load().cz_selftest_bounded_wait(int(timeout_ns), _ptr(workspace),
+                                                                       _stream_ptr(stream)))
