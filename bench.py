@@ -401,6 +401,16 @@ def main():
                 "frac": ach / hbm if hbm else None, "traffic": traffic, "algorithmic_per_launch": per_launch,
                 "launch_ms": avg_ms, "peak_source": f"hbm_gbs of {peak_src}"}
 
+    # planner timing on the 64-layer Qwen3-32B layout (host work, as the pages' "milliseconds" claim)
+    full = wl.qwen3_32b_reverse()
+    fb = cz.cz_make_buckets(full.numels, full.bucket_cap)
+    t0 = time.perf_counter()
+    p32 = cz.cz_plan_partition(full.numels, fb, full.R, full.alpha)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    planner = {"layout": "qwen3-32b 64 layers, 448 tensors, 320 buckets, R=32, alpha=1", "alg1_ms": plan_ms,
+               "r_lb": p32.metrics()["r_lb"], "naive_r_lb": cz.cz_plan_naive(full.numels, fb, full.R).metrics()["r_lb"],
+               "shard_plan": plan.metrics()}
+
     if rank == 0:
         cpu = None
         if not args.no_cpu_baseline and world == 1:
@@ -428,7 +438,7 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clk, "wall_s_timed_region": wall,
-            "planner": plan.metrics(),
+            "planner": planner,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -70,6 +70,15 @@ int cz_plan_partition(const int64_t* numels, int64_t n_params,
                       const int64_t* bucket_sizes, int64_t n_buckets,
                       int32_t R, double alpha, cz_plan** out);
 
+/* Algorithm 1 with an explicit cost W(p) per parameter (costs[n_params], positive),
+ * e.g. the Newton-Schulz FLOPs of each tensor -- the non-linear cost the pages'
+ * appendix D.5 compares with numel.  Loads, deficits and cut targets are in cost
+ * units; shard sizes (elem cuts, J_Comm) stay in elements.  costs = NULL is
+ * cz_plan_partition. */
+int cz_plan_partition_cost(const int64_t* numels, const int64_t* costs, int64_t n_params,
+                           const int64_t* bucket_sizes, int64_t n_buckets,
+                           int32_t R, double alpha, cz_plan** out);
+
 /* Eq. 1, the start-index split: parameter p at element offset o inside bucket
  * B_i goes to rank floor(o * R / |B_i|), i.e. r*S <= o < (r+1)*S, S = |B_i|/R. */
 int cz_plan_naive(const int64_t* numels, int64_t n_params,
@@ -89,12 +98,31 @@ int cz_plan_owner(const cz_plan* plan, int32_t* owner_out);
  * (element offsets within the bucket).  Either pointer may be NULL. */
 int cz_plan_cuts(const cz_plan* plan, int64_t* param_cuts, int64_t* elem_cuts);
 
-/* load_out[R]: elements owned by each rank (sum over buckets of L_{i,r}). */
+/* load_out[R]: load owned by each rank, sum over buckets of L_{i,r}, in cost
+ * units (elements for cz_plan_partition / cz_plan_naive). */
 int cz_plan_rank_load(const cz_plan* plan, int64_t* load_out);
+
+/* elems_out[R]: elements (memory) owned by each rank. */
+int cz_plan_rank_elems(const cz_plan* plan, int64_t* elems_out);
 
 /* R_LB = max_r L_r / mean; J_DP = max_r |L_r - mu| (Eq. 2); J_Comm =
  * sum_i sum_r |S_{i,r} - |B_i|/R|.  Any pointer may be NULL. */
 int cz_plan_metrics(const cz_plan* plan, double* r_lb, double* j_dp, double* j_comm);
+
+/* TP Micro-Group Construction with Greedy Rollback and the MinHeapSolver
+ * (section 3.4, "The TP Hierarchical Partitioning and Scheduling"): the
+ * n_params TP-split tensors with positive costs W(p) are sorted by (W, ID)
+ * descending and packed into groups in that order; a tensor joins the current
+ * group if the LPT assignment of the group to R host ranks (min-heap of
+ * (load, rank), ties to the smaller rank) keeps the largest rank load <= c_max,
+ * otherwise the group is finalised and the tensor starts the next one (a tensor
+ * whose cost alone exceeds c_max forms a group of its own).
+ *   group_out[n_params]: group index of each tensor, groups numbered in order;
+ *   host_out[n_params]:  host rank of each tensor within its group;
+ *   *n_groups_out:       number of groups.
+ * Integer arithmetic only: identical on every rank. */
+int cz_plan_microgroups(const int64_t* costs, int64_t n_params, int32_t R, int64_t c_max,
+                        int32_t* group_out, int32_t* host_out, int64_t* n_groups_out);
 
 /* Options of the Muon step.  Fill with cz_step_opts_default, then override. */
 typedef struct {

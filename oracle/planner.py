@@ -63,49 +63,59 @@ class Plan:
     R: int
     bucket_sizes: List[int]                 # params per bucket
     param_cuts: List[List[int]]             # per bucket, s_{i,0..R} in parameter indices
-    elem_cuts: List[List[int]]              # per bucket, Phi_i(s_{i,r}) (element offsets)
+    elem_cuts: List[List[int]]              # per bucket, element offsets of the cuts
     owner: List[int] = field(default_factory=list)       # per parameter, 0-based rank
     rank_load: List[int] = field(default_factory=list)   # sum of W(p) per rank
+    rank_elems: List[int] = field(default_factory=list)  # sum of numel(p) per rank
 
 
-def _bucket_prefix(numels: Sequence[int], bucket_sizes: Sequence[int]):
-    """Per bucket: its parameters' W(p) = numel(p) and Phi_i(u) for u = 0..n_i."""
+def _bucket_prefix(numels: Sequence[int], bucket_sizes: Sequence[int], costs=None):
+    """Per bucket: its parameters' costs W(p) (numel(p) unless given), Phi_i(u)
+    for u = 0..n_i in cost units, and the element prefix for the same cuts."""
     out = []
     pos = 0
     for nb in bucket_sizes:
-        w = [int(x) for x in numels[pos:pos + nb]]
+        e = [int(x) for x in numels[pos:pos + nb]]
+        w = e if costs is None else [int(x) for x in costs[pos:pos + nb]]
         phi = [0]
         for x in w:
             phi.append(phi[-1] + x)
-        out.append((pos, w, phi))
+        ephi = [0]
+        for x in e:
+            ephi.append(ephi[-1] + x)
+        out.append((pos, w, phi, ephi))
         pos += nb
     return out
 
 
-def _check(numels, bucket_sizes, R):
+def _check(numels, bucket_sizes, R, costs=None):
     if R < 1:
         raise ValueError("R must be >= 1")
     if any(int(x) <= 0 for x in numels):
         raise ValueError("numel must be positive")
+    if costs is not None and (len(costs) != len(numels) or any(int(x) <= 0 for x in costs)):
+        raise ValueError("costs must be positive, one per parameter")
     if any(int(b) <= 0 for b in bucket_sizes):
         raise ValueError("bucket sizes must be positive")
     if sum(int(b) for b in bucket_sizes) != len(numels):
         raise ValueError("bucket sizes must cover all parameters")
 
 
-def _finish(numels, bucket_sizes, R, param_cuts, elem_cuts) -> Plan:
+def _finish(numels, bucket_sizes, R, param_cuts, elem_cuts, costs=None) -> Plan:
     owner = [0] * len(numels)
     load = [0] * R
+    elems = [0] * R
     pos = 0
     for i, nb in enumerate(bucket_sizes):
         s = param_cuts[i]
         for r in range(R):
             for u in range(s[r], s[r + 1]):
                 owner[pos + u] = r
-                load[r] += int(numels[pos + u])
+                load[r] += int(numels[pos + u] if costs is None else costs[pos + u])
+                elems[r] += int(numels[pos + u])
         pos += nb
     return Plan(R=R, bucket_sizes=list(bucket_sizes), param_cuts=param_cuts,
-                elem_cuts=elem_cuts, owner=owner, rank_load=load)
+                elem_cuts=elem_cuts, owner=owner, rank_load=load, rank_elems=elems)
 
 
 def plan_naive(numels: Sequence[int], bucket_sizes: Sequence[int], R: int) -> Plan:
@@ -116,7 +126,7 @@ def plan_naive(numels: Sequence[int], bucket_sizes: Sequence[int], R: int) -> Pl
     """
     _check(numels, bucket_sizes, R)
     param_cuts, elem_cuts = [], []
-    for _, w, phi in _bucket_prefix(numels, bucket_sizes):
+    for _, w, phi, _ in _bucket_prefix(numels, bucket_sizes):
         size = phi[-1]
         owners = [(phi[u] * R) // size for u in range(len(w))]
         # s_{i,r} = first parameter whose owner is >= r
@@ -134,12 +144,15 @@ def plan_naive(numels: Sequence[int], bucket_sizes: Sequence[int], R: int) -> Pl
 
 
 def plan_partition(numels: Sequence[int], bucket_sizes: Sequence[int], R: int,
-                   alpha: float) -> Plan:
-    """Algorithm 1, alpha-Balanced Greedy LPT, cost W(p) = numel(p)."""
-    _check(numels, bucket_sizes, R)
+                   alpha: float, costs: Sequence[int] = None) -> Plan:
+    """Algorithm 1, alpha-Balanced Greedy LPT.  Cost W(p) = numel(p) by default; any
+    positive integer cost per parameter (e.g. the Newton-Schulz FLOPs of the tensor,
+    the non-linear cost of the pages' appendix D.5) can be given instead.  Loads,
+    deficits and cut targets are in cost units; shard sizes stay in elements."""
+    _check(numels, bucket_sizes, R, costs)
     if not (0.0 <= alpha <= 1.0):
         raise ValueError("alpha must lie in [0, 1]")
-    buckets = _bucket_prefix(numels, bucket_sizes)
+    buckets = _bucket_prefix(numels, bucket_sizes, costs)
     N = len(buckets)
     Wb = [b[2][-1] for b in buckets]                 # W^i, exact ints
     total = 0
@@ -180,8 +193,8 @@ def plan_partition(numels: Sequence[int], bucket_sizes: Sequence[int], R: int,
         s[R] = nk
         L[R - 1] += float(phi[s[R]] - phi[s[R - 1]])
         param_cuts[k] = s
-    elem_cuts = [[buckets[i][2][u] for u in param_cuts[i]] for i in range(N)]
-    return _finish(numels, bucket_sizes, R, param_cuts, elem_cuts)
+    elem_cuts = [[buckets[i][3][u] for u in param_cuts[i]] for i in range(N)]
+    return _finish(numels, bucket_sizes, R, param_cuts, elem_cuts, costs)
 
 
 def metrics(plan: Plan) -> dict:

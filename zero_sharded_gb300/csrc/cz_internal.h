@@ -22,14 +22,16 @@ struct Plan : cz_plan {
   int64_t n_params = 0, n_buckets = 0;
   int kind = 0;              // 0: Algorithm 1, 1: Eq. 1 start-index split
   double alpha = 0.0;
-  std::vector<int64_t> numels, bucket_sizes;
+  std::vector<int64_t> numels, costs, bucket_sizes;   // costs = W(p) (numels unless given)
   std::vector<int64_t> bucket_first;   // first parameter of each bucket (+ end)
-  std::vector<int64_t> phi_first;      // start of each bucket's Phi in `phi` (+ end)
-  std::vector<int64_t> phi;            // Phi_i(u), u = 0..n_i, concatenated
+  std::vector<int64_t> phi_first;      // start of each bucket's prefixes in `phi`/`cphi` (+ end)
+  std::vector<int64_t> phi;            // element prefix per bucket, u = 0..n_i, concatenated
+  std::vector<int64_t> cphi;           // cost prefix Phi_i(u), same layout
   std::vector<int64_t> param_cuts;     // n_buckets*(R+1)
   std::vector<int64_t> elem_cuts;      // n_buckets*(R+1)
   std::vector<int32_t> owner;          // n_params
-  std::vector<int64_t> rank_load;      // R
+  std::vector<int64_t> rank_load;      // R, in cost units
+  std::vector<int64_t> rank_elems;     // R, elements
   double r_lb = 0, j_dp = 0, j_comm = 0;
 };
 

@@ -27,11 +27,11 @@ uint64_t next_uid() {
 namespace {
 
 int check_inputs(const int64_t* numels, int64_t n_params, const int64_t* bucket_sizes,
-                 int64_t n_buckets, int32_t R) {
+                 int64_t n_buckets, int32_t R, const int64_t* costs = nullptr) {
   if (!numels || !bucket_sizes || n_params <= 0 || n_buckets <= 0 || R < 1) return CZ_ERR_INVALID;
   int64_t sum = 0;
   for (int64_t i = 0; i < n_params; ++i)
-    if (numels[i] <= 0) return CZ_ERR_INVALID;
+    if (numels[i] <= 0 || (costs && costs[i] <= 0)) return CZ_ERR_INVALID;
   for (int64_t i = 0; i < n_buckets; ++i) {
     if (bucket_sizes[i] <= 0) return CZ_ERR_INVALID;
     sum += bucket_sizes[i];
@@ -40,20 +40,24 @@ int check_inputs(const int64_t* numels, int64_t n_params, const int64_t* bucket_
   return sum == n_params ? CZ_OK : CZ_ERR_INVALID;
 }
 
-// Per-bucket prefix Phi_i(u), u = 0..n_i, in one flat array.
+// Per-bucket prefixes, u = 0..n_i, in flat arrays: elements (phi) and cost units (cphi).
 void build_prefix(Plan& p) {
   p.bucket_first.resize(p.n_buckets + 1);
   p.phi_first.resize(p.n_buckets + 1);
   p.phi.clear();
+  p.cphi.clear();
   int64_t pos = 0;
   for (int64_t i = 0; i < p.n_buckets; ++i) {
     p.bucket_first[i] = pos;
     p.phi_first[i] = (int64_t)p.phi.size();
-    int64_t acc = 0;
+    int64_t acc = 0, cacc = 0;
     p.phi.push_back(0);
+    p.cphi.push_back(0);
     for (int64_t u = 0; u < p.bucket_sizes[i]; ++u) {
       acc += p.numels[pos + u];
+      cacc += p.costs[pos + u];
       p.phi.push_back(acc);
+      p.cphi.push_back(cacc);
     }
     pos += p.bucket_sizes[i];
   }
@@ -66,6 +70,7 @@ void finish(Plan& p) {
   const int32_t R = p.R;
   p.owner.assign(p.n_params, 0);
   p.rank_load.assign(R, 0);
+  p.rank_elems.assign(R, 0);
   p.elem_cuts.assign(p.n_buckets * (R + 1), 0);
   for (int64_t i = 0; i < p.n_buckets; ++i) {
     const int64_t* s = &p.param_cuts[i * (R + 1)];
@@ -74,7 +79,8 @@ void finish(Plan& p) {
     for (int32_t r = 0; r < R; ++r) {
       for (int64_t u = s[r]; u < s[r + 1]; ++u) {
         p.owner[base + u] = r;
-        p.rank_load[r] += p.numels[base + u];
+        p.rank_load[r] += p.costs[base + u];
+        p.rank_elems[r] += p.numels[base + u];
       }
     }
     for (int32_t r = 0; r <= R; ++r) p.elem_cuts[i * (R + 1) + r] = phi[s[r]];
@@ -100,13 +106,15 @@ void finish(Plan& p) {
 }
 
 Plan* new_plan(const int64_t* numels, int64_t n_params, const int64_t* bucket_sizes,
-               int64_t n_buckets, int32_t R) {
+               int64_t n_buckets, int32_t R, const int64_t* costs = nullptr) {
   Plan* p = new (std::nothrow) Plan();
   if (!p) return nullptr;
   p->R = R;
   p->n_params = n_params;
   p->n_buckets = n_buckets;
   p->numels.assign(numels, numels + n_params);
+  if (costs) p->costs.assign(costs, costs + n_params);
+  else p->costs = p->numels;
   p->bucket_sizes.assign(bucket_sizes, bucket_sizes + n_buckets);
   build_prefix(*p);
   p->param_cuts.assign(n_buckets * (R + 1), 0);
@@ -169,12 +177,18 @@ int cz_plan_naive(const int64_t* numels, int64_t n_params, const int64_t* bucket
 
 int cz_plan_partition(const int64_t* numels, int64_t n_params, const int64_t* bucket_sizes,
                       int64_t n_buckets, int32_t R, double alpha, cz_plan** out) {
+  return cz_plan_partition_cost(numels, nullptr, n_params, bucket_sizes, n_buckets, R, alpha, out);
+}
+
+int cz_plan_partition_cost(const int64_t* numels, const int64_t* costs, int64_t n_params,
+                           const int64_t* bucket_sizes, int64_t n_buckets, int32_t R, double alpha,
+                           cz_plan** out) {
   if (!out) return CZ_ERR_INVALID;
   *out = nullptr;
-  int st = check_inputs(numels, n_params, bucket_sizes, n_buckets, R);
+  int st = check_inputs(numels, n_params, bucket_sizes, n_buckets, R, costs);
   if (st != CZ_OK) return st;
   if (!(alpha >= 0.0 && alpha <= 1.0)) return CZ_ERR_INVALID;
-  Plan* p = new_plan(numels, n_params, bucket_sizes, n_buckets, R);
+  Plan* p = new_plan(numels, n_params, bucket_sizes, n_buckets, R, costs);
   if (!p) return CZ_ERR_NOMEM;
   p->kind = 0;
   p->alpha = alpha;
@@ -182,7 +196,7 @@ int cz_plan_partition(const int64_t* numels, int64_t n_params, const int64_t* bu
   std::vector<int64_t> Wb(n_buckets);
   int64_t total = 0;
   for (int64_t i = 0; i < n_buckets; ++i) {
-    Wb[i] = p->phi[p->phi_first[i] + bucket_sizes[i]];
+    Wb[i] = p->cphi[p->phi_first[i] + bucket_sizes[i]];
     total += Wb[i];
   }
   const double mu = (double)total / (double)R;
@@ -196,7 +210,7 @@ int cz_plan_partition(const int64_t* numels, int64_t n_params, const int64_t* bu
   std::vector<double> L(R, 0.0), d(R), t(R);
   for (int64_t k : order) {
     const int64_t nk = bucket_sizes[k];
-    const int64_t* phi = &p->phi[p->phi_first[k]];
+    const int64_t* phi = &p->cphi[p->phi_first[k]];   // Phi_k(u) in cost units
     // step 1: deficits at the start of this bucket
     double D = 0.0;
     for (int32_t r = 0; r < R; ++r) {
@@ -276,6 +290,13 @@ int cz_plan_rank_load(const cz_plan* plan, int64_t* load_out) {
   if (!plan || !load_out) return CZ_ERR_INVALID;
   const Plan* p = static_cast<const Plan*>(plan);
   std::copy(p->rank_load.begin(), p->rank_load.end(), load_out);
+  return CZ_OK;
+}
+
+int cz_plan_rank_elems(const cz_plan* plan, int64_t* elems_out) {
+  if (!plan || !elems_out) return CZ_ERR_INVALID;
+  const Plan* p = static_cast<const Plan*>(plan);
+  std::copy(p->rank_elems.begin(), p->rank_elems.end(), elems_out);
   return CZ_OK;
 }
 

@@ -71,6 +71,11 @@ def load() -> ctypes.CDLL:
                                              ctypes.c_double, ctypes.POINTER(ctypes.c_void_p)]),
         "cz_plan_naive": (ctypes.c_int, [_i64p, ctypes.c_int64, _i64p, ctypes.c_int64, ctypes.c_int32,
                                          ctypes.POINTER(ctypes.c_void_p)]),
+        "cz_plan_partition_cost": (ctypes.c_int, [_i64p, _i64p, ctypes.c_int64, _i64p, ctypes.c_int64,
+                                                  ctypes.c_int32, ctypes.c_double, ctypes.POINTER(ctypes.c_void_p)]),
+        "cz_plan_rank_elems": (ctypes.c_int, [ctypes.c_void_p, _i64p]),
+        "cz_plan_microgroups": (ctypes.c_int, [_i64p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, _i32p, _i32p,
+                                               _i64p]),
         "cz_plan_free": (None, [ctypes.c_void_p]),
         "cz_plan_info": (ctypes.c_int, [ctypes.c_void_p, _i64p, _i64p, _i32p]),
         "cz_plan_owner": (ctypes.c_int, [ctypes.c_void_p, _i32p]),
@@ -187,6 +192,12 @@ class Plan:
         _check("cz_plan_rank_load", load().cz_plan_rank_load(self._h, out))
         return list(out)
 
+    def rank_elems(self) -> List[int]:
+        _, _, R = self.info()
+        out = (ctypes.c_int64 * R)()
+        _check("cz_plan_rank_elems", load().cz_plan_rank_elems(self._h, out))
+        return list(out)
+
     def metrics(self) -> dict:
         r, j, c = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
         _check("cz_plan_metrics", load().cz_plan_metrics(self._h, ctypes.byref(r), ctypes.byref(j), ctypes.byref(c)))
@@ -199,6 +210,27 @@ def cz_plan_partition(numels: Sequence[int], bucket_sizes: Sequence[int], R: int
     _check("cz_plan_partition", lib.cz_plan_partition(_i64(numels), len(numels), _i64(bucket_sizes),
                                                       len(bucket_sizes), int(R), float(alpha), ctypes.byref(h)))
     return Plan(h.value)
+
+
+def cz_plan_partition_cost(numels: Sequence[int], costs: Sequence[int], bucket_sizes: Sequence[int], R: int,
+                           alpha: float) -> Plan:
+    lib = load()
+    h = ctypes.c_void_p()
+    _check("cz_plan_partition_cost", lib.cz_plan_partition_cost(_i64(numels), _i64(costs), len(numels),
+                                                                _i64(bucket_sizes), len(bucket_sizes), int(R),
+                                                                float(alpha), ctypes.byref(h)))
+    return Plan(h.value)
+
+
+def cz_plan_microgroups(costs: Sequence[int], R: int, c_max: int) -> Tuple[List[int], List[int], int]:
+    """Returns (group index per tensor, host rank per tensor, number of groups)."""
+    n = len(costs)
+    g = (ctypes.c_int32 * max(1, n))()
+    h = (ctypes.c_int32 * max(1, n))()
+    ng = ctypes.c_int64(0)
+    _check("cz_plan_microgroups", load().cz_plan_microgroups(_i64(costs), n, int(R), int(c_max), g, h,
+                                                             ctypes.byref(ng)))
+    return list(g[:n]), list(h[:n]), ng.value
 
 
 def cz_plan_naive(numels: Sequence[int], bucket_sizes: Sequence[int], R: int) -> Plan:
