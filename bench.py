@@ -401,6 +401,31 @@ def main():
                 "frac": ach / hbm if hbm else None, "traffic": traffic, "algorithmic_per_launch": per_launch,
                 "launch_ms": avg_ms, "peak_source": f"hbm_gbs of {peak_src}"}
 
+    # variable-size collective support: pack + unpack of the gradient buffer as one bucket whose shards are
+    # whole tensors (cuts at tensor boundaries, as a partition map gives), blocks rounded to 16 bytes
+    el_all = G.numel()
+    cuts8 = list(w.offsets) + [el_all]
+    nsh = len(cuts8) - 1
+    blk = max(cuts8[i + 1] - cuts8[i] for i in range(nsh))
+    blk = (blk + 7) // 8 * 8
+    padded = torch.empty(nsh * blk, dtype=G.dtype, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    with torch.cuda.stream(stream):
+        cz.cz_bucket_pack(G, cuts8, blk, padded, stream)
+        cz.cz_bucket_unpack(padded, cuts8, blk, G, stream)
+        ev[0].record(stream)
+        cz.cz_bucket_pack(G, cuts8, blk, padded, stream)
+        ev[1].record(stream)
+        cz.cz_bucket_unpack(padded, cuts8, blk, G, stream)
+        ev[2].record(stream)
+    torch.cuda.synchronize()
+    esz = G.element_size()
+    pack_ms, unpack_ms = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+    comm_pack = {"bucket_elements": el_all, "ranks": nsh, "block": blk,
+                 "pack_gbs": (el_all + nsh * blk) * esz / (pack_ms * 1e-3) / 1e9,
+                 "unpack_gbs": 2 * el_all * esz / (unpack_ms * 1e-3) / 1e9}
+    del padded
+
     # planner timing on the 64-layer Qwen3-32B layout (host work, as the pages' "milliseconds" claim)
     full = wl.qwen3_32b_reverse()
     fb = cz.cz_make_buckets(full.numels, full.bucket_cap)
@@ -438,7 +463,7 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clk, "wall_s_timed_region": wall,
-            "planner": planner,
+            "planner": planner, "comm_pack": comm_pack,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

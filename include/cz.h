@@ -124,6 +124,23 @@ int cz_plan_metrics(const cz_plan* plan, double* r_lb, double* j_dp, double* j_c
 int cz_plan_microgroups(const int64_t* costs, int64_t n_params, int32_t R, int64_t c_max,
                         int32_t* group_out, int32_t* host_out, int64_t* n_groups_out);
 
+/* Variable-size collectives around the step (section 3.4, "Runtime Static-Layout
+ * Enforcement": bucket B_i is reduce-scattered and all-gathered with per-rank
+ * sizes S_{i,r} taken from the partition map).  Primitives that need equal
+ * counts per rank take R blocks of `block` >= max_r S_{i,r} elements:
+ *   cz_bucket_pack:   padded[r*block + j] = bucket[elem_cuts[r] + j] for j < S_{i,r},
+ *                     0 for S_{i,r} <= j < block  (before a ReduceScatter);
+ *   cz_bucket_unpack: bucket[elem_cuts[r] + j] = padded[r*block + j] for j < S_{i,r}
+ *                     (after an AllGather); padding is ignored.
+ * bucket / padded: device buffers of elem_bytes-byte elements (1, 2, 4 or 8;
+ * values are copied bit for bit).  elem_cuts: host, R+1 element offsets within the
+ * bucket (one row of cz_plan_cuts' elem_cuts), elem_cuts[0] = 0, non-decreasing.
+ * R <= 1024.  Asynchronous on `stream`. */
+int cz_bucket_pack(const void* bucket, int32_t elem_bytes, const int64_t* elem_cuts, int32_t R,
+                   int64_t block, void* padded, void* stream);
+int cz_bucket_unpack(const void* padded, int32_t elem_bytes, const int64_t* elem_cuts, int32_t R,
+                     int64_t block, void* bucket, void* stream);
+
 /* Options of the Muon step.  Fill with cz_step_opts_default, then override. */
 typedef struct {
   int32_t nesterov;        /* 1: u = g + mu*m (default); 0: u = m                       */

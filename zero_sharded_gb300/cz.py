@@ -98,6 +98,10 @@ def load() -> ctypes.CDLL:
         "cz_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
         "cz_profile_read": (ctypes.c_int, [_f64p, _i64p, ctypes.c_int32]),
         "cz_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
+        "cz_bucket_pack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _i64p, ctypes.c_int32, ctypes.c_int64,
+                                          ctypes.c_void_p, ctypes.c_void_p]),
+        "cz_bucket_unpack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _i64p, ctypes.c_int32, ctypes.c_int64,
+                                            ctypes.c_void_p, ctypes.c_void_p]),
         "cz_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "cz_version": (ctypes.c_char_p, []),
     }
@@ -340,3 +344,17 @@ def cz_profile_read() -> dict:
 def cz_selftest_bounded_wait(timeout_ns: int, workspace, stream=None) -> None:
     _check("cz_selftest_bounded_wait", load().cz_selftest_bounded_wait(int(timeout_ns), _ptr(workspace),
                                                                        _stream_ptr(stream)))
+
+
+def cz_bucket_pack(bucket, elem_cuts: Sequence[int], block: int, padded, stream=None) -> None:
+    """Rank r's interval of the bucket -> block r of `padded` (zero tail)."""
+    R = len(elem_cuts) - 1
+    _check("cz_bucket_pack", load().cz_bucket_pack(_ptr(bucket), int(bucket.element_size()), _i64(elem_cuts), R,
+                                                   int(block), _ptr(padded), _stream_ptr(stream)))
+
+
+def cz_bucket_unpack(padded, elem_cuts: Sequence[int], block: int, bucket, stream=None) -> None:
+    """Block r of `padded` (first S_r elements) -> rank r's interval of the bucket."""
+    R = len(elem_cuts) - 1
+    _check("cz_bucket_unpack", load().cz_bucket_unpack(_ptr(padded), int(padded.element_size()), _i64(elem_cuts), R,
+                                                       int(block), _ptr(bucket), _stream_ptr(stream)))
