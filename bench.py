@@ -45,7 +45,8 @@ def ns_flops_by_kind(shapes, steps=NS_STEPS):
     """Algorithmic flops per step of each GEMM kernel kind (the product each launch computes)."""
     g = sum(2 * min(r, c) ** 2 * max(r, c) for r, c in shapes)
     p = sum(2 * min(r, c) ** 3 for r, c in shapes)
-    return {"ns_gram": steps * g, "ns_poly": steps * p, "ns_update": (steps - 1) * g, "ns_update_apply": g}
+    return {"ns_gram": steps * g, "ns_poly": steps * p, "ns_update": (steps - 1) * g, "ns_update_apply": g,
+            "ns_fused": steps * (2 * g + p)}
 
 
 def ns_flops_executed(shapes, steps=NS_STEPS, bm=128, bn=256):
@@ -338,7 +339,7 @@ def main():
     prof = cz.cz_profile_read()
     cz.cz_profile_enable(False)
     launches_per_step = sum(c for _, c in prof.values()) / args.steps
-    ns_kinds = ("ns_gram", "ns_poly", "ns_update", "ns_update_apply")
+    ns_kinds = ("ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused")
     ns_ms = sum(prof[k][0] for k in ns_kinds) / args.steps
     ns_launch = sum(prof[k][1] for k in ns_kinds) / args.steps
     mom_ms = prof["momentum"][0] / args.steps

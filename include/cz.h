@@ -227,9 +227,10 @@ int cz_device_status(void* stream, void* workspace, int* status_out);
  * cz_profile_read synchronises on them and returns, per kernel kind, the summed
  * milliseconds and launch counts since the previous read (then clears them).
  * Kinds, in order: 0 momentum pass, 1 norm finalize, 2 Gram (A = X X^T),
- * 3 Poly (B = bA + cA^2), 4 Update (X <- aX + BX), 5 Update fused with the apply.
+ * 3 Poly (B = bA + cA^2), 4 Update (X <- aX + BX), 5 Update fused with the apply,
+ * 6 all Newton-Schulz products of a step in one launch (the default).
  * ms and launches must hold n_kinds entries (n_kinds <= CZ_KERNEL_KINDS). */
-#define CZ_KERNEL_KINDS 6
+#define CZ_KERNEL_KINDS 7
 int cz_profile_enable(int32_t on);
 int cz_profile_read(double* ms, int64_t* launches, int32_t n_kinds);
 

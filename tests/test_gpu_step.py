@@ -212,3 +212,46 @@ def test_caller_workspace_reused_between_calls():
         assert torch.equal(a.P.cpu(), b.P.cpu())
         assert torch.equal(a.M.cpu(), b.M.cpu())
         WS[256:].fill_(0xA5)        # scribble over everything but the status word
+
+
+_PER_PRODUCT_CHILD = r"""
+import sys, numpy as np, torch
+from zero_sharded_gb300 import cz
+from zero_sharded_gb300 import workloads as wl
+shapes = [(384, 1024), (1024, 384), (256, 256), (128, 640)]
+numels = [r * c for r, c in shapes]
+offsets = list(np.cumsum([0] + numels[:-1]))
+plan = cz.cz_plan_partition(numels, [len(shapes)], 1, 1.0)
+P = wl.draw(shapes, 0.02, 31).cuda()
+G = wl.draw(shapes, 1.0, 32).cuda()
+M = torch.zeros_like(P)
+cz.cz_profile_enable(True)
+for _ in range(2):
+    cz.cz_muon_step(plan, 0, P, G, M, cz.StepArgs(offsets, shapes), 0.02, 0.95, 5)
+torch.cuda.synchronize()
+prof = cz.cz_profile_read()
+assert cz.cz_device_status(None, None) == cz.CZ_OK
+torch.save({"P": P.cpu(), "M": M.cpu(), "fused": prof["ns_fused"][1], "gram": prof["ns_gram"][1]}, sys.argv[1])
+"""
+
+
+def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
+    """One persistent launch for all Newton-Schulz products and one launch per product
+    compute every output tile with the same K order and epilogue: bit-identical
+    results after two steps.  Each variant runs in its own process (the choice is
+    read once per process)."""
+    import os
+    import subprocess
+    import sys
+    outs = {}
+    for env in ("1", "0"):
+        f = tmp_path / f"out_{env}.pt"
+        e = dict(os.environ, CZ_NS_FUSED=env)
+        r = subprocess.run([sys.executable, "-c", _PER_PRODUCT_CHILD, str(f)], env=e, capture_output=True,
+                           text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs[env] = torch.load(f)
+    assert outs["1"]["fused"] == 2 and outs["1"]["gram"] == 0        # the small shard takes the fused launch
+    assert outs["0"]["fused"] == 0 and outs["0"]["gram"] >= 10       # >= one Gram launch per NS step
+    assert torch.equal(outs["1"]["P"], outs["0"]["P"])
+    assert torch.equal(outs["1"]["M"], outs["0"]["M"])

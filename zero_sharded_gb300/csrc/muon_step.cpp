@@ -32,6 +32,7 @@ namespace {
 
 constexpr int64_t kAlign = 256;
 constexpr int64_t kDefaultTimeoutNs = 1000000000LL;   // 1 s per device-side wait
+constexpr int64_t kMaxNsSteps = 64;
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -63,6 +64,8 @@ struct Layout {
   int64_t n_gemm_tiles = 0;
   int64_t off_cta = 0;             // per launch: grid+1 tile offsets (int32)
   int64_t n_cta_entries = 0;
+  int64_t off_expect = 0;          // fused launch: n_mats x 3 expected arrivals (int32)
+  int64_t off_done = 0;            // fused launch: 3 x kMaxNsSteps x n_mats counters (int32)
   int64_t bytes = 0;
 };
 
@@ -149,6 +152,8 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
                            2 * ceil_div64(std::max<int64_t>(2 * G, 1), kMaxProblems);
   L.n_cta_entries = n_launch * (kMaxGrid + 1);
   L.off_cta = off; off = align_up(off + 4 * L.n_cta_entries, kAlign);
+  L.off_expect = off; off = align_up(off + 4 * 3 * std::max<int64_t>(n_mats, 1), kAlign);
+  L.off_done = off; off = align_up(off + 4 * 3 * kMaxNsSteps * std::max<int64_t>(n_mats, 1), kAlign);
   for (Group& G : L.groups) {
     G.ldx = align_up(G.n, 8);
     G.ldm = align_up(G.m, 8);
@@ -171,6 +176,24 @@ bool use_pair() {
     return !(e && e[0] == '0');
   }();
   return pair;
+}
+
+// All Newton-Schulz products of a step in one persistent launch with per-matrix
+// dependencies (default); CZ_NS_FUSED=0 launches each product separately.
+bool use_fused() {
+  static const bool fused = [] {
+    const char* e = std::getenv("CZ_NS_FUSED");
+    return !(e && e[0] == '0');
+  }();
+  return fused;
+}
+
+// L2 size of the current device, in bytes (0 if it cannot be read).
+int64_t l2_bytes() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+  return v;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -215,6 +238,8 @@ struct Launch {
 struct Program {
   uint64_t uid = next_uid();
   bool pair = true;
+  bool fused_ok = false;
+  GemmParams fused{};
   Layout L;
   std::vector<uint8_t> host_tables;   // image of [off_sigma .. off_tiles + tiles) region (tables only)
   int64_t tables_begin = 0, tables_end = 0;
@@ -311,7 +336,8 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
     }
     if (tl.empty()) continue;
     std::stable_sort(tl.begin(), tl.end(), [](const TileRef& x, const TileRef& y) { return x.cost > y.cost; });
-    const int grid = (int)std::min<int64_t>((int64_t)tl.size(), std::min(max_grid, kMaxGrid));
+    // every list of a program uses the same unit count, so a fused launch can walk them all
+    const int grid = std::min(max_grid, kMaxGrid);
     std::vector<std::vector<int4>> per(grid);
     {
       // min-heap of (load, cta)
@@ -367,7 +393,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   if (st != CZ_OK) return st;
   const int64_t n_mats = (int64_t)L.mats.size();
   P.tables_begin = L.off_sigma;
-  P.tables_end = L.off_cta + 4 * L.n_cta_entries;
+  P.tables_end = L.off_expect + 4 * 3 * (int64_t)std::max<size_t>(L.mats.size(), 1);
   P.host_tables.assign((size_t)(P.tables_end - P.tables_begin), 0);
   auto& img = P.host_tables;
   const int64_t tb = P.tables_begin;
@@ -467,6 +493,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       // Gram: A = s^2 X X^T, stored with its mirror into A
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.n; d.gp.count = c; d.gp.mat_base = G.mat_base;
+      d.gp.phase = kGram; d.gp.slot = 0;
       if (!encode_map(&d.ta, X, G.n, G.m, c, G.ldx, msx, kBM) || !encode_map(&d.tb, X, G.n, G.m, c, G.ldx, msx, b_box) ||
           !encode_map(&d.to, A, G.m, G.m, c, G.ldm, msa, 0, true))
         return CZ_ERR_CUDA;
@@ -478,6 +505,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       // Poly: B' = a I + b A + c A A, stored with its mirror into B
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
+      d.gp.phase = kPoly; d.gp.slot = 1;
       d.gp.aux = A; d.gp.ld_aux = G.ldm; d.gp.ms_aux = msa;
       if (!encode_map(&d.ta, A, G.m, G.m, c, G.ldm, msa, kBM) || !encode_map(&d.tb, A, G.m, G.m, c, G.ldm, msa, b_box) ||
           !encode_map(&d.to, B, G.m, G.m, c, G.ldm, msa, 0, true))
@@ -491,6 +519,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       // stores X and X^T (into the other ping-pong buffer)
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.n; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
+      d.gp.phase = kUpdate; d.gp.slot = 2;
       if (!encode_map(&d.ta, B, G.m, G.m, c, G.ldm, msa, kBM) ||
           !encode_map(&d.tb, XT[cur], G.m, G.n, c, G.ldm, mst, b_box) ||
           !encode_map(&d.to, X, G.n, G.m, c, G.ldx, msx, 0, true) ||
@@ -505,6 +534,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       if (G.has_wide) {
         ProbDesc e = d;
         e.gp.orient = 0;
+        e.gp.phase = kApply;
         e.tiles.clear();
         for (int j = 0; j < c; ++j) {
           if (L.mats[G.mat_base + j].tall) continue;
@@ -517,6 +547,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         ProbDesc e{};
         e.gp.M = G.n; e.gp.N = G.m; e.gp.K = G.m; e.gp.count = c; e.gp.mat_base = G.mat_base;
         e.gp.orient = 1;
+        e.gp.phase = kApply; e.gp.slot = 2;
         if (!encode_map(&e.ta, XT[cur], G.m, G.n, c, G.ldm, mst, kBM) ||
             !encode_map(&e.tb, B, G.m, G.m, c, G.ldm, msa, b_box))
           return CZ_ERR_CUDA;
@@ -545,6 +576,57 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   (void)ns_steps;
   // cannot happen: both regions are sized by build_layout
   if (cursor > L.n_gemm_tiles || cta_cursor > L.n_cta_entries) return CZ_ERR_NOMEM;
+
+  // expected arrivals per (matrix, slot): tiles of the matrix x epilogue warps per unit
+  const int arrivals = kEpiWarps * (pair ? 2 : 1);
+  int32_t* expect = at<int32_t>(img, tb, L.off_expect);
+  for (auto& pd : gram)
+    for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 0] += arrivals;
+  for (auto& pd : poly)
+    for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 1] += arrivals;
+  for (auto& pd : upd[0])
+    for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 2] += arrivals;
+
+  // fused launch: one problem table over the six lists, each list walked per unit
+  const std::vector<Launch>* lists[kFusedLists] = {&P.gram, &P.poly, &P.update[0], &P.update[1], &P.apply[0],
+                                                   &P.apply[1]};
+  bool ok_fused = true;
+  int total = 0;
+  for (auto* v : lists) {
+    if (v->size() != 1) ok_fused = false;
+    else total += (*v)[0].params.n_prob;
+  }
+  // The fused launch runs the products of all matrices side by side, so it pays only
+  // while the shard's bf16 iterate fits the L2: larger shards keep their L2 reuse
+  // better with one launch per product in grouped raster order.
+  int64_t x_bytes = 0;
+  for (const Group& G : L.groups) x_bytes += 2 * (int64_t)G.m * G.n * G.count;
+  if (ok_fused && total <= kMaxProblems && x_bytes <= l2_bytes()) {
+    GemmParams& F = P.fused;
+    F = common;
+    int off = 0;
+    for (int li = 0; li < kFusedLists; ++li) {
+      const GemmParams& q = (*lists[li])[0].params;
+      for (int i = 0; i < q.n_prob; ++i) {
+        F.tmA[off + i] = q.tmA[i];
+        F.tmB[off + i] = q.tmB[i];
+        F.tmO[off + i] = q.tmO[i];
+        F.tmOT[off + i] = q.tmOT[i];
+        F.prob[off + i] = q.prob[i];
+      }
+      F.lists[li].tiles = q.tiles;
+      F.lists[li].cta_first = q.cta_first;
+      F.lists[li].prob_off = off;
+      F.grid = q.grid;
+      off += q.n_prob;
+    }
+    F.n_prob = total;
+    F.n_tiles = 1;   // non-zero: the launch is not skipped
+    F.n_mats = (int32_t)n_mats;
+    F.expect = reinterpret_cast<const int*>(ws + L.off_expect);
+    F.done = reinterpret_cast<int*>(ws + L.off_done);
+    P.fused_ok = true;
+  }
   return CZ_OK;
 }
 
@@ -693,6 +775,15 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
   if (traced(0, s, [&] { return launch_momentum(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
   if (traced(1, s, [&] { return launch_sigma_finalize(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
   GemmParams gp;
+  if (P.fused_ok && use_fused() && ns_steps <= kMaxNsSteps) {
+    if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + P.L.off_done, 0,
+                        (size_t)4 * 3 * ns_steps * std::max<size_t>(P.L.mats.size(), 1), s) != cudaSuccess)
+      return CZ_ERR_CUDA;
+    gp = P.fused;
+    gp.ns_steps = ns_steps;
+    if (traced(6, s, [&] { return launch_ns_gemm(kFused, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+    return CZ_OK;
+  }
   for (int t = 0; t < ns_steps; ++t) {
     const int first = t == 0 ? 1 : 0;
     const int cur = t & 1;

@@ -224,6 +224,178 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProbl
   }
 }
 
+// The tiles a unit (CTA or CTA pair) processes, in order.  A per-phase launch
+// walks its own range of p.tiles.  The fused launch walks, for every Newton-Schulz
+// step, the unit's ranges of the Gram, Poly and Update (Apply in the last step)
+// lists, so all three roles see the same sequence without a fused tile list.
+template <int PHASE>
+struct Walker {
+  const GemmParams& p;
+  const int unit;
+  int it = 0, slot = 0, j = 0, j_end = 0;
+  bool open = false;
+  __device__ Walker(const GemmParams& p_, int unit_) : p(p_), unit(unit_) {}
+  __device__ int list_of(int i, int sl) const {
+    return sl == 0 ? 0 : sl == 1 ? 1 : (i + 1 == p.ns_steps ? 4 : 2) + (i & 1);
+  }
+  // Next tile: its entry, global problem index, Newton-Schulz step and slot.
+  __device__ bool next(int4& tl, int& prob, int& iter, int& sl) {
+    if constexpr (PHASE != kFused) {
+      if (!open) {
+        j = p.cta_first[unit];
+        j_end = p.cta_first[unit + 1];
+        open = true;
+      }
+      if (j >= j_end) return false;
+      tl = p.tiles[j++];
+      prob = tl.x;
+      iter = 0;
+      sl = 0;
+      return true;
+    } else {
+      while (true) {
+        const TileList& L = p.lists[list_of(it, slot)];
+        if (!open) {
+          j = L.cta_first[unit];
+          j_end = L.cta_first[unit + 1];
+          open = true;
+        }
+        if (j < j_end) {
+          tl = L.tiles[j++];
+          prob = L.prob_off + tl.x;
+          iter = it;
+          sl = slot;
+          return true;
+        }
+        open = false;
+        if (++slot == 3) {
+          slot = 0;
+          if (++it == p.ns_steps) return false;
+        }
+      }
+    }
+  }
+};
+
+// Completion counter and arrivals of the stage a fused tile depends on
+// (previous slot of the same Newton-Schulz step, or the last slot of the step before).
+__device__ __forceinline__ bool fused_dependency(const GemmParams& p, int gm, int iter, int sl, const int** ctr,
+                                                 int* target) {
+  if (iter == 0 && sl == 0) return false;
+  const int ps = sl == 0 ? 2 : sl - 1;
+  const int pit = sl == 0 ? iter - 1 : iter;
+  *ctr = p.done + (size_t)(pit * 3 + ps) * p.n_mats + gm;
+  *target = p.expect[gm * 3 + ps];
+  return true;
+}
+
+struct EpiCtx {
+  uint64_t* tfull;
+  uint64_t* tempty;
+  volatile int* abort;
+  uint32_t tmem_base, lane_field;
+  int quad, half, lane;
+  uint32_t rank;
+  __nv_bfloat16* stD;
+  __nv_bfloat16* stT;
+  bool pending;           // bulk stores in flight from the staging blocks
+};
+
+// Epilogue of one tile in phase PH: prefetch the first chunk's operands, wait for
+// the accumulator, then per 32-column chunk read TMEM, apply the phase math and
+// store; the accumulator is handed back after its last read.  Symmetric outputs
+// (Gram, Poly) are written by aligned 32 x 32 blocks: a block above the diagonal
+// directly and mirrored, a diagonal block directly, a block below not at all (its
+// mirror comes from the block above), so each element is written exactly once.
+// Returns false if the wait for the accumulator ran out.
+template <int PH, bool PAIR>
+__device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, const GemmProblem& pr, int prob,
+                                              int mat, int tile_m, int tile_n, bool first, uint32_t acc,
+                                              uint32_t acc_phase) {
+  using C = Cfg<PAIR>;
+  constexpr bool kSym = PH == kGram || PH == kPoly;
+  const int lane = e.lane;
+  const int gm = pr.mat_base + mat;
+  const int rbase = tile_m * C::kTileM + (int)e.rank * 128 + e.quad * 32;
+  const int ch_first = e.half * 4;
+  const int col_first = tile_n * kBN + ch_first * 32;
+  auto release = [&]() {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&e.tempty[acc]), 0));
+      else mbar_arrive(&e.tempty[acc]);
+    }
+  };
+  // chunks this warp reads from TMEM (warp-uniform bit mask)
+  uint32_t need = 0;
+  if (rbase < pr.M) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int col0 = col_first + c * 32;
+      if (col0 < pr.N && (!kSym || rbase <= col0)) need |= 1u << c;
+    }
+  }
+  const int last = need ? 31 - __clz(need) : -1;
+  float s = 1.f;
+  if (first) {
+    const float sg = p.sigma[gm];
+    s = (PH == kGram) ? sg * sg : sg;
+  }
+  MatInfo mi{};
+  if constexpr (PH == kApply) mi = p.mats[gm];
+  Pre cur;
+  const int first_c = need ? __ffs(need) - 1 : 0;
+  if (need) prefetch<PH>(cur, p, pr, mat, mi, rbase, lane, col_first + first_c * 32);
+  const bool w = mbar_wait(&e.tfull[acc], acc_phase, e.abort, p.status, p.timeout_ns);
+  if (!__all_sync(0xffffffffu, w)) return false;
+  tc_fence_after();
+  const uint32_t tbase = e.tmem_base + acc * (uint32_t)kBN + e.lane_field;
+  if (last < 0) release();
+  for (int c = first_c; c <= last; ++c) {
+    if (!((need >> c) & 1u)) continue;
+    const int col0 = col_first + c * 32;
+    Pre nxt;
+    const uint32_t later = need >> (c + 1);
+    if (later) prefetch<PH>(nxt, p, pr, mat, mi, rbase, lane, col0 + 32 * __ffs(later));
+    float v[32];
+    tmem_ld32(tbase + (uint32_t)((ch_first + c) * 32), v);
+    if (c == last) release();     // accumulator no longer needed: let the MMA reuse it
+    if constexpr (PH == kApply) {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) v[q] *= s;
+      apply_chunk(p, pr, mi, rbase, col0, v, cur, reinterpret_cast<float*>(e.stD), lane);
+    } else {
+      if constexpr (PH == kPoly) {
+        // B' = a I + b A + c (A A)
+        float a[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) unpack8(cur.x[q], a + 8 * q);
+        const bool diag = rbase == col0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = fmaf(p.b, a[q], p.c * v[q]) + ((diag && q == lane) ? p.a : 0.f);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] *= s;   // Gram: s = sigma^2; Update: s = sigma (step 1)
+      }
+      const bool do_t = !kSym || rbase < col0;
+      if (lane == 0 && e.pending) bulk_wait_read_all();
+      __syncwarp();
+      stage_block(e.stD, e.stT, v, lane, do_t);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&p.tmO[prob], e.stD, col0, rbase, mat);
+        if (do_t) tma_store_3d(&p.tmOT[prob], e.stT, rbase, col0, mat);
+        bulk_commit();
+        e.pending = true;
+      }
+    }
+    cur = nxt;
+  }
+  return true;
+}
+
 template <int PHASE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<PAIR>;
@@ -258,9 +430,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *sm.tmem_holder;
-  // this unit's tiles (host LPT assignment, heaviest first)
-  const int t_begin = p.cta_first[unit];
-  const int t_end = p.cta_first[unit + 1];
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer (both CTAs of a pair)
@@ -268,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       for (int i = 0; i < p.n_prob; ++i) {
         tma_prefetch_desc(&p.tmA[i]);
         tma_prefetch_desc(&p.tmB[i]);
-        if (PHASE != kApply) {
+        if (PHASE != kApply && p.prob[i].phase != kApply) {   // Apply problems store no tiles
           tma_prefetch_desc(&p.tmO[i]);
           tma_prefetch_desc(&p.tmOT[i]);
         }
@@ -276,11 +445,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;   // bit s: parity of stage s's last fill
     bool ok = true;
-    for (int t = t_begin; t < t_end && ok; ++t) {
-      const int4 tl = p.tiles[t];
-      const int nk = ceil_div(p.prob[tl.x].K, kBK);
-      const CUtensorMap* ma = &p.tmA[tl.x];
-      const CUtensorMap* mb = &p.tmB[tl.x];
+    Walker<PHASE> walk(p, unit);
+    int4 tl;
+    int prob, iter, sl;
+    while (ok && walk.next(tl, prob, iter, sl)) {
+      const GemmProblem& pr = p.prob[prob];
+      if constexpr (PHASE == kFused) {
+        // the matrix's previous stage must be complete (and visible) before its data is loaded
+        const int* ctr;
+        int target;
+        if (fused_dependency(p, pr.mat_base + tl.y, iter, sl, &ctr, &target)) {
+          bool w = true;
+          if (lane == 0) w = counter_wait(ctr, target, abort, p.status, p.timeout_ns);
+          if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
+        }
+      }
+      const int nk = ceil_div(pr.K, kBK);
+      const CUtensorMap* ma = &p.tmA[prob];
+      const CUtensorMap* mb = &p.tmB[prob];
       const int arow = tl.z * C::kTileM + (int)rank * 128;
       const int brow = tl.w * kBN + (int)rank * C::kRowsB;
       for (int kb = 0; kb < nk; ++kb) {
@@ -329,9 +511,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       constexpr uint32_t idesc = idesc_bf16_f32(C::kTileM, kBN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = t_begin; t < t_end && ok; ++t) {
-        const int4 tl = p.tiles[t];
-        const int nk = ceil_div(p.prob[tl.x].K, kBK);
+      Walker<PHASE> walk(p, unit);
+      int4 tl;
+      int prob, iter, sl;
+      while (ok && walk.next(tl, prob, iter, sl)) {
+        const int nk = ceil_div(p.prob[prob].K, kBK);
         bool w = true;
         if (lane == 0) w = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort, p.status, p.timeout_ns);
         if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
@@ -381,106 +565,65 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
   } else {
     // ---------------------------------------------------------- epilogue (both CTAs of a pair)
-    // Symmetric outputs (Gram, Poly) are written by aligned 32 x 32 blocks: a
-    // block above the diagonal is stored directly and mirrored, a diagonal block
-    // directly only, a block below the diagonal not at all (its mirror comes from
-    // the block above), so each element is written exactly once.
-    constexpr bool kSym = PHASE == kGram || PHASE == kPoly;
     const int ew = warp - 2;                    // 0 .. kEpiWarps-1
-    const int quad = warp & 3;                  // TMEM lane quarter this warp may access
-    const int half = ew >> 2;                   // which 128 of the 256 accumulator columns
-    __nv_bfloat16* stD = sm.epi + ew * (kEpiBytesPerWarp / 2);
-    __nv_bfloat16* stT = stD + 32 * 32;
-    const uint32_t lane_field = (uint32_t)(quad * 32) << 16;
+    EpiCtx e;
+    e.tfull = sm.tfull;
+    e.tempty = sm.tempty;
+    e.abort = abort;
+    e.tmem_base = tmem_base;
+    e.quad = warp & 3;                          // TMEM lane quarter this warp may access
+    e.half = ew >> 2;                           // which 128 of the 256 accumulator columns
+    e.lane = lane;
+    e.rank = rank;
+    e.lane_field = (uint32_t)(e.quad * 32) << 16;
+    e.stD = sm.epi + ew * (kEpiBytesPerWarp / 2);
+    e.stT = e.stD + 32 * 32;
+    e.pending = false;
     uint32_t acc = 0, acc_phase = 0;
-    bool pending = false;                       // bulk stores in flight from the staging blocks
-    // the accumulator buffer is handed back to the MMA issuer (even CTA) once per warp
-    auto release = [&](uint32_t buf) {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(&sm.tempty[buf]), 0));
-        else mbar_arrive(&sm.tempty[buf]);
-      }
-    };
-    for (int t = t_begin; t < t_end; ++t) {
-      const int4 tl = p.tiles[t];
-      const GemmProblem& pr = p.prob[tl.x];
-      const int mat = tl.y;
-      const int gm = pr.mat_base + mat;
-      const int rbase = tl.z * C::kTileM + (int)rank * 128 + quad * 32;
-      const int ch_first = half * 4;
-      const int col_first = tl.w * kBN + ch_first * 32;
-      // chunks this warp reads from TMEM (warp-uniform bit mask)
-      uint32_t need = 0;
-      if (rbase < pr.M) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int col0 = col_first + c * 32;
-          if (col0 < pr.N && (!kSym || rbase <= col0)) need |= 1u << c;
-        }
-      }
-      const int last = need ? 31 - __clz(need) : -1;
-      float s = 1.f;
-      if (p.first) {
-        const float sg = p.sigma[gm];
-        s = (PHASE == kGram) ? sg * sg : sg;
-      }
-      MatInfo mi{};
-      if constexpr (PHASE == kApply) mi = p.mats[gm];
-      Pre cur;
-      const int first_c = need ? __ffs(need) - 1 : 0;
-      if (need) prefetch<PHASE>(cur, p, pr, mat, mi, rbase, lane, col_first + first_c * 32);
-      const bool w = mbar_wait(&sm.tfull[acc], acc_phase, abort, p.status, p.timeout_ns);
-      if (!__all_sync(0xffffffffu, w)) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + acc * (uint32_t)kBN + lane_field;
-      if (last < 0) release(acc);
-      for (int c = first_c; c <= last; ++c) {
-        if (!((need >> c) & 1u)) continue;
-        const int col0 = col_first + c * 32;
-        Pre nxt;
-        const uint32_t later = need >> (c + 1);
-        if (later) prefetch<PHASE>(nxt, p, pr, mat, mi, rbase, lane, col0 + 32 * __ffs(later));
-        float v[32];
-        tmem_ld32(tbase + (uint32_t)((ch_first + c) * 32), v);
-        if (c == last) release(acc);     // accumulator no longer needed: let the MMA reuse it
-        if constexpr (PHASE == kApply) {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] *= s;
-          apply_chunk(p, pr, mi, rbase, col0, v, cur, reinterpret_cast<float*>(stD), lane);
-        } else {
-          if constexpr (PHASE == kPoly) {
-            // B' = a I + b A + c (A A)
-            float a[32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) unpack8(cur.x[q], a + 8 * q);
-            const bool diag = rbase == col0;
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = fmaf(p.b, a[q], p.c * v[q]) + ((diag && q == lane) ? p.a : 0.f);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] *= s;   // Gram: s = sigma^2; Update: s = sigma (step 1)
+    Walker<PHASE> walk(p, unit);
+    int4 tl;
+    int prob, iter, sl;
+    while (walk.next(tl, prob, iter, sl)) {
+      const GemmProblem& pr = p.prob[prob];
+      bool ok;
+      if constexpr (PHASE == kFused) {
+        const bool first = iter == 0;
+        switch (pr.phase) {
+          case kGram: ok = epilogue_tile<kGram, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase); break;
+          case kPoly: {
+            // the Poly epilogue reads A directly: acquire the Gram stage it depends on
+            const int* ctr;
+            int target;
+            if (fused_dependency(p, pr.mat_base + tl.y, iter, sl, &ctr, &target))
+              counter_wait(ctr, target, abort, p.status, p.timeout_ns);
+            ok = epilogue_tile<kPoly, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase);
+            break;
           }
-          const bool do_t = !kSym || rbase < col0;
-          if (lane == 0 && pending) bulk_wait_read_all();
-          __syncwarp();
-          stage_block(stD, stT, v, lane, do_t);
-          fence_proxy_async_smem();
-          __syncwarp();
+          case kUpdate:
+            ok = epilogue_tile<kUpdate, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase);
+            break;
+          default: ok = epilogue_tile<kApply, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase); break;
+        }
+        // publish this warp's part of the tile once its stores are complete; the
+        // last step's Apply has no successor
+        if (ok && !(sl == 2 && iter + 1 == p.ns_steps)) {
           if (lane == 0) {
-            tma_store_3d(&p.tmO[tl.x], stD, col0, rbase, mat);
-            if (do_t) tma_store_3d(&p.tmOT[tl.x], stT, rbase, col0, mat);
-            bulk_commit();
-            pending = true;
+            if (e.pending) {
+              bulk_wait_all();
+              e.pending = false;
+            }
+            counter_release_add(p.done + (size_t)(iter * 3 + sl) * p.n_mats + pr.mat_base + tl.y, 1);
           }
+          __syncwarp();
         }
-        cur = nxt;
+      } else {
+        ok = epilogue_tile<PHASE, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, p.first != 0, acc, acc_phase);
       }
+      if (!ok) break;
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0 && pending) bulk_wait_all();
+    if (lane == 0 && e.pending) bulk_wait_all();
     __syncwarp();
   }
 
@@ -539,6 +682,8 @@ cudaError_t launch_ns_gemm(int phase, bool pair, const GemmParams& p, cudaStream
     case kUpdate * 2 + 1: return launch_phase<kUpdate, true>(p, s);
     case kApply * 2: return launch_phase<kApply, false>(p, s);
     case kApply * 2 + 1: return launch_phase<kApply, true>(p, s);
+    case kFused * 2: return launch_phase<kFused, false>(p, s);
+    case kFused * 2 + 1: return launch_phase<kFused, true>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }

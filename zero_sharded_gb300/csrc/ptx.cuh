@@ -83,6 +83,44 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ---------------------------------------------------------------- cross-CTA dependency counters
+// Publish: the caller's async-proxy writes (completed TMA stores) are ordered
+// before the release-add at GPU scope.
+__device__ __forceinline__ void counter_release_add(int* ctr, int v) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+__device__ __forceinline__ int counter_acquire_load(const int* ctr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  return v;
+}
+// Waits until *ctr >= target (acquire), then orders later async-proxy reads (TMA
+// loads) after it.  Bounded like mbar_wait.
+__device__ __forceinline__ bool counter_wait(const int* ctr, int target, volatile int* abort, int* status,
+                                             int64_t timeout_ns) {
+  if (counter_acquire_load(ctr) >= target) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    if (counter_acquire_load(ctr) >= target) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if ((it & 63u) == 0) {
+      if (abort && *abort) return false;
+      if ((int64_t)(globaltimer_ns() - t0) > timeout_ns) {
+        record_status(status, CZ_ERR_TIMEOUT);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -52,7 +52,7 @@ constexpr int kBM = 128;        // UMMA M (TMEM lanes)
 constexpr int kBN = 256;        // UMMA N (TMEM columns per accumulator)
 constexpr int kBK = 64;         // 64 bf16 = one 128-byte swizzle row
 constexpr int kStages = 4;
-constexpr int kMaxProblems = 16;
+constexpr int kMaxProblems = 32;
 constexpr int kMaxGrid = 1024;  // upper bound on the persistent grid (SM count)
 
 enum Phase : int32_t {
@@ -60,6 +60,7 @@ enum Phase : int32_t {
   kPoly = 1,     // B' = a I + b A + c A A          (symmetric output)
   kUpdate = 2,   // X <- s B' X, also writes X^T     (= s (a X + B X))
   kApply = 3,    // last step: W <- W - lr*scale*s B' X  (+ bf16 copy, debug delta)
+  kFused = 4,    // every product of all ns_steps in one launch, per-matrix dependencies
 };
 
 // One batched GEMM: `count` matrices of the same M x N x K, operands read by
@@ -69,7 +70,8 @@ struct GemmProblem {
   int32_t M, N, K, count;
   int32_t mat_base;       // global index (sigma / MatInfo) of matrix 0 of this problem
   int32_t orient;         // kApply: 0 -> output is X (m x n), 1 -> output is X^T (n x m)
-  int32_t pad0, pad1;
+  int32_t phase;          // kGram .. kApply (read by the fused launch)
+  int32_t slot;           // position in a Newton-Schulz step: 0 Gram, 1 Poly, 2 Update/Apply
   const uint16_t* aux;   int64_t ld_aux, ms_aux;     // kPoly: A (for the b A term)
 };
 
@@ -80,6 +82,15 @@ struct MatInfo {
   float lrs;              // lr * sqrt(max(1, rows/cols))
   int32_t vec_ok;         // w_off and cols are multiples of 4 (16-byte fp32 vectors)
 };
+
+// One phase's tile list inside a fused launch.
+struct TileList {
+  const int4* tiles;          // {problem (index within the list's problems), matrix, tile_m, tile_n}
+  const int32_t* cta_first;   // grid+1 entries, as GemmParams::cta_first
+  int32_t prob_off;           // the list's problem 0 in GemmParams::prob
+  int32_t pad;
+};
+constexpr int kFusedLists = 6;  // Gram, Poly, Update (X^T buffer 0), Update (1), Apply (0), Apply (1)
 
 struct GemmParams {
   CUtensorMap tmA[kMaxProblems];    // A-side operand loads (128 x 64 boxes, 128-byte swizzle)
@@ -101,6 +112,12 @@ struct GemmParams {
   float* dbg;             // debug delta or null (kApply)
   int* status;
   int64_t timeout_ns;
+  // fused launch (kFused) only
+  int32_t ns_steps;
+  int32_t n_mats;
+  TileList lists[kFusedLists];
+  int* done;              // (3 * ns_steps) x n_mats completion counters, zero at launch
+  const int* expect;      // n_mats x 3: arrivals that complete (matrix, slot)
 };
 
 // Dynamic shared memory of the GEMM kernel.
