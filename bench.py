@@ -41,21 +41,37 @@ def ns_flops(shapes, steps=NS_STEPS):
     return tot
 
 
+SMALL_M, SMALL_N = 128, 256     # matrices whose Newton-Schulz steps run on chip (ns_small)
+
+
+def _is_small(r, c):
+    return min(r, c) <= SMALL_M and max(r, c) <= SMALL_N
+
+
 def ns_flops_by_kind(shapes, steps=NS_STEPS):
     """Algorithmic flops per step of each GEMM kernel kind (the product each launch computes)."""
-    g = sum(2 * min(r, c) ** 2 * max(r, c) for r, c in shapes)
-    p = sum(2 * min(r, c) ** 3 for r, c in shapes)
+    tiled = [s for s in shapes if not _is_small(*s)]
+    small = [s for s in shapes if _is_small(*s)]
+    g = sum(2 * min(r, c) ** 2 * max(r, c) for r, c in tiled)
+    p = sum(2 * min(r, c) ** 3 for r, c in tiled)
+    gs = sum(2 * min(r, c) ** 2 * max(r, c) for r, c in small)
+    ps = sum(2 * min(r, c) ** 3 for r, c in small)
     return {"ns_gram": steps * g, "ns_poly": steps * p, "ns_update": (steps - 1) * g, "ns_update_apply": g,
-            "ns_fused": steps * (2 * g + p)}
+            "ns_fused": steps * (2 * g + p), "ns_small": steps * (2 * gs + ps)}
 
 
 def ns_flops_executed(shapes, steps=NS_STEPS, bm=128, bn=256):
-    """Flops the tensor cores execute: 128x256 tiles, symmetric products on upper tiles only."""
+    """Flops the tensor cores execute: 128x256 tiles, symmetric products on upper tiles only;
+    on-chip small matrices as 128-row products with n padded to 64."""
     def cdiv(a, b):
         return (a + b - 1) // b
     tot = 0
     for r, c in shapes:
         m, n = min(r, c), max(r, c)
+        if _is_small(r, c):
+            n_pad = cdiv(n, 64) * 64
+            tot += steps * (2 * 128 * 128 * n_pad + 2 * 128 * 128 * 128 + 2 * 128 * n_pad * 128)
+            continue
         sym = sum(1 for a in range(cdiv(m, bm)) for b in range(cdiv(m, bn)) if a * bm <= b * bn + bn - 1)
         kpad_n, kpad_m = cdiv(n, 64) * 64, cdiv(m, 64) * 64
         gram = sym * 2 * bm * bn * kpad_n
@@ -339,7 +355,7 @@ def main():
     prof = cz.cz_profile_read()
     cz.cz_profile_enable(False)
     launches_per_step = sum(c for _, c in prof.values()) / args.steps
-    ns_kinds = ("ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused")
+    ns_kinds = ("ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused", "ns_small")
     ns_ms = sum(prof[k][0] for k in ns_kinds) / args.steps
     ns_launch = sum(prof[k][1] for k in ns_kinds) / args.steps
     mom_ms = prof["momentum"][0] / args.steps

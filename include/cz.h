@@ -228,9 +228,10 @@ int cz_device_status(void* stream, void* workspace, int* status_out);
  * milliseconds and launch counts since the previous read (then clears them).
  * Kinds, in order: 0 momentum pass, 1 norm finalize, 2 Gram (A = X X^T),
  * 3 Poly (B = bA + cA^2), 4 Update (X <- aX + BX), 5 Update fused with the apply,
- * 6 all Newton-Schulz products of a step in one launch (the default).
+ * 6 all Newton-Schulz products of a step in one launch (the default),
+ * 7 every Newton-Schulz step of the small matrices (m <= 128, n <= 256) on chip.
  * ms and launches must hold n_kinds entries (n_kinds <= CZ_KERNEL_KINDS). */
-#define CZ_KERNEL_KINDS 7
+#define CZ_KERNEL_KINDS 8
 int cz_profile_enable(int32_t on);
 int cz_profile_read(double* ms, int64_t* launches, int32_t n_kinds);
 

@@ -175,3 +175,32 @@ def test_ns_flops_formula():
     # q/k/v/o/gate/up/down of one Qwen3-1.7B layer: 2.43 TFLOP for 5 steps
     tot = sum(M.ns_flops(r, c) for r, c in wl.qwen3_1p7b_layers(1).shapes)
     assert tot == pytest.approx(2.43e12, rel=0.01)
+
+
+def test_bf16_model_without_rounding_is_the_oracle_iteration():
+    """The rounding model runs the oracle's iteration (only storage precision differs):
+    with rounding off it matches the fp64 oracle to 1e-12 on ragged, tall and wide shapes."""
+    from tests.bf16_model import orthogonalise_bf16
+    rng = np.random.default_rng(11)
+    for r, c in [(3, 256), (40, 17), (64, 64), (7, 1)]:
+        u = rng.standard_normal((r, c))
+        for steps in (1, 5):
+            want = M.orthogonalise(u, steps)
+            got = orthogonalise_bf16(u, steps, rounding=False)
+            assert np.linalg.norm(got - want) <= 1e-12 * np.linalg.norm(want)
+
+
+def test_bf16_storage_alone_can_exceed_the_update_bar():
+    """A Gaussian 3 x 256 gradient: its normalised singular values all sit near 1/sqrt(3),
+    f maps them near 1.2 where f' ~ 3.9, and bf16 storage alone (the rounding model)
+    lands more than 2e-2 from the fp64 oracle after 5 steps, while 1 step stays well inside."""
+    from tests.bf16_model import orthogonalise_bf16
+    a, b, c = M.QUINTIC
+    x = M.ns_poly_scalar(1 / np.sqrt(3), steps=1)
+    assert 1.15 < x < 1.25 and a + 3 * b * x * x + 5 * c * x ** 4 > 3.0
+    rng = np.random.default_rng(5)
+    u = rng.standard_normal((3, 256))
+    e5 = np.linalg.norm(orthogonalise_bf16(u, 5) - M.orthogonalise(u, 5)) / np.linalg.norm(M.orthogonalise(u, 5))
+    e1 = np.linalg.norm(orthogonalise_bf16(u, 1) - M.orthogonalise(u, 1)) / np.linalg.norm(M.orthogonalise(u, 1))
+    assert e1 < 1e-2
+    assert e5 > 1.5e-2

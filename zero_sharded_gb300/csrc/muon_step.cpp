@@ -53,6 +53,7 @@ struct Group {
   int64_t ldx = 0, ldm = 0;    // element pitches: X rows (n), X^T / A / B rows (m)
   int64_t off_x = 0, off_xt[2] = {0, 0}, off_a = 0, off_b = 0;   // workspace byte offsets
   bool has_wide = false, has_tall = false;
+  bool small = false;          // every Newton-Schulz step on chip (ns_small), no tiled GEMMs
 };
 
 struct Layout {
@@ -60,6 +61,8 @@ struct Layout {
   std::vector<Group> groups;
   int64_t n_mom_tiles = 0;
   int64_t off_status = 0, off_sigma = 0, off_partial = 0, off_momtiles = 0, off_mommats = 0, off_matinfo = 0;
+  int64_t off_small = 0;           // SmallMat per matrix of the small groups
+  int32_t n_small = 0;
   int64_t off_tiles = 0;           // all GEMM tile lists
   int64_t n_gemm_tiles = 0;
   int64_t off_cta = 0;             // per launch: grid+1 tile offsets (int32)
@@ -68,6 +71,16 @@ struct Layout {
   int64_t off_done = 0;            // fused launch: 3 x kMaxNsSteps x n_mats counters (int32)
   int64_t bytes = 0;
 };
+
+// Small groups (m <= 128, n <= 256) take the on-chip kernel (default);
+// CZ_NS_SMALL=0 sends them through the tiled GEMMs like every other group.
+bool use_small() {
+  static const bool small = [] {
+    const char* e = std::getenv("CZ_NS_SMALL");
+    return !(e && e[0] == '0');
+  }();
+  return small;
+}
 
 int validate_shapes(const Plan* p, const int64_t* shapes) {
   for (int64_t i = 0; i < p->n_params; ++i) {
@@ -117,6 +130,8 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
       G.has_wide |= !om.tall;
       L.mats.push_back(om);
     }
+    G.small = use_small() && G.m <= kSmallMaxM && G.n <= kSmallMaxN;
+    if (G.small) L.n_small += G.count;
     base += G.count;
   }
   // workspace layout
@@ -129,10 +144,12 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   L.off_momtiles = off; off = align_up(off + (int64_t)sizeof(MomTile) * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
   L.off_mommats = off; off = align_up(off + (int64_t)sizeof(MomMat) * std::max<int64_t>(n_mats, 1), kAlign);
   L.off_matinfo = off; off = align_up(off + (int64_t)sizeof(MatInfo) * std::max<int64_t>(n_mats, 1), kAlign);
+  L.off_small = off;   off = align_up(off + (int64_t)sizeof(SmallMat) * std::max<int64_t>(L.n_small, 1), kAlign);
   // GEMM tiles: Gram + Poly (same count), and two ping-pong copies each of the
   // Update and Apply lists (a tall tensor's Apply tiles cover n x m)
   int64_t nt = 0;
   for (const Group& G : L.groups) {
+    if (G.small) continue;
     const int64_t tm = ceil_div64(G.m, kBM), tn = ceil_div64(G.m, kBN);
     int64_t sym = 0;
     for (int64_t a = 0; a < tm; ++a)
@@ -245,6 +262,7 @@ struct Program {
   int64_t tables_begin = 0, tables_end = 0;
   MomParams mom{};
   std::vector<Launch> gram, poly, update[2], apply[2];
+  SmallParams small{};
 };
 
 struct Key {
@@ -476,7 +494,23 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   const uint32_t b_box = pair ? 128 : kBN;       // B-side rows each CTA loads per stage
   const int max_grid = gemm_max_units(pair);
   std::vector<ProbDesc> gram, poly, upd[2], app[2];
+  SmallMat* smt = at<SmallMat>(img, tb, L.off_small);
+  int32_t n_small = 0;
   for (const Group& G : L.groups) {
+    if (G.small) {
+      for (int j = 0; j < G.count; ++j) {
+        SmallMat& e = smt[n_small++];
+        e.x = reinterpret_cast<const uint16_t*>(ws + G.off_x) + (int64_t)j * G.m * G.ldx;
+        e.xt = reinterpret_cast<const uint16_t*>(ws + G.off_xt[0]) + (int64_t)j * G.n * G.ldm;
+        e.ldx = (int32_t)G.ldx;
+        e.ldm = (int32_t)G.ldm;
+        e.m = G.m;
+        e.n = G.n;
+        e.mat = G.mat_base + j;
+        e.pad = 0;
+      }
+      continue;
+    }
     uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x);
     uint16_t* XT[2] = {reinterpret_cast<uint16_t*>(ws + G.off_xt[0]), reinterpret_cast<uint16_t*>(ws + G.off_xt[1])};
     uint16_t* A = reinterpret_cast<uint16_t*>(ws + G.off_a);
@@ -574,6 +608,20 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     ml(kApply, app[cur], P.apply[cur], cur);
   }
   (void)ns_steps;
+  SmallParams& sp = P.small;
+  sp.mats = reinterpret_cast<const SmallMat*>(ws + L.off_small);
+  sp.n_mats = n_small;
+  sp.ns_steps = 0;                // set per call
+  sp.sigma = mp.sigma;
+  sp.info = common.mats;
+  sp.a = o.a;
+  sp.b = o.b;
+  sp.c = o.c;
+  sp.W = flat_param;
+  sp.Wb = common.Wb;
+  sp.dbg = o.debug_update_out;
+  sp.status = mp.status;
+  sp.timeout_ns = kDefaultTimeoutNs;
   // cannot happen: both regions are sized by build_layout
   if (cursor > L.n_gemm_tiles || cta_cursor > L.n_cta_entries) return CZ_ERR_NOMEM;
 
@@ -600,7 +648,8 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   // while the shard's bf16 iterate fits the L2: larger shards keep their L2 reuse
   // better with one launch per product in grouped raster order.
   int64_t x_bytes = 0;
-  for (const Group& G : L.groups) x_bytes += 2 * (int64_t)G.m * G.n * G.count;
+  for (const Group& G : L.groups)
+    if (!G.small) x_bytes += 2 * (int64_t)G.m * G.n * G.count;
   if (ok_fused && total <= kMaxProblems && x_bytes <= l2_bytes()) {
     GemmParams& F = P.fused;
     F = common;
@@ -774,6 +823,11 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
   const Program& P = *prog;
   if (traced(0, s, [&] { return launch_momentum(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
   if (traced(1, s, [&] { return launch_sigma_finalize(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+  if (P.small.n_mats > 0) {
+    SmallParams sp = P.small;
+    sp.ns_steps = ns_steps;
+    if (traced(7, s, [&] { return launch_ns_small(sp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+  }
   GemmParams gp;
   if (P.fused_ok && use_fused() && ns_steps <= kMaxNsSteps) {
     if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + P.L.off_done, 0,

@@ -134,4 +134,36 @@ constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageBytesA + 
 cudaError_t launch_ns_gemm(int phase, bool pair, const GemmParams& p, cudaStream_t s);
 int gemm_max_units(bool pair);   // units that can be resident at once (persistent grid bound)
 
+// ------------------------------------------------------------------ small-matrix Newton-Schulz
+// Matrices with m <= kSmallMaxM and n <= kSmallMaxN run every Newton-Schulz step
+// in one CTA with X, X^T, A and B' resident in shared memory and the accumulators
+// in TMEM (one CTA per matrix, one launch for all of them).
+constexpr int kSmallMaxM = 128;
+constexpr int kSmallMaxN = 256;
+
+struct SmallMat {
+  const uint16_t* x;      // bf16 X (m x n), row pitch ldx (written by the momentum pass)
+  const uint16_t* xt;     // bf16 X^T (n x m), row pitch ldm
+  int32_t ldx, ldm;
+  int32_t m, n;
+  int32_t mat;            // global matrix index (sigma, MatInfo)
+  int32_t pad;
+};
+
+struct SmallParams {
+  const SmallMat* mats;
+  int32_t n_mats;
+  int32_t ns_steps;
+  const float* sigma;     // per global matrix
+  const MatInfo* info;    // per global matrix
+  float a, b, c;
+  float* W;               // fp32 master
+  uint16_t* Wb;           // bf16 copy or null
+  float* dbg;             // debug delta or null
+  int* status;
+  int64_t timeout_ns;
+};
+
+cudaError_t launch_ns_small(const SmallParams& p, cudaStream_t s);
+
 }  // namespace cz

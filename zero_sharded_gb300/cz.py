@@ -326,7 +326,8 @@ def cz_device_status(stream=None, workspace=None) -> int:
     return v.value
 
 
-KERNEL_KINDS = ("momentum", "norm_finalize", "ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused")
+KERNEL_KINDS = ("momentum", "norm_finalize", "ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused",
+                "ns_small")
 
 
 def cz_profile_enable(on: bool) -> None:
