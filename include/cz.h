@@ -226,7 +226,8 @@ int cz_device_status(void* stream, void* workspace, int* status_out);
  * launches is bracketed by two CUDA events recorded on the caller's stream;
  * cz_profile_read synchronises on them and returns, per kernel kind, the summed
  * milliseconds and launch counts since the previous read (then clears them).
- * Kinds, in order: 0 momentum pass, 1 norm finalize, 2 Gram (A = X X^T),
+ * Kinds, in order: 0 momentum pass (including the per-tensor norm), 1 not launched
+ * (kept so the numbering stays stable), 2 Gram (A = X X^T),
  * 3 Poly (B = bA + cA^2), 4 Update (X <- aX + BX), 5 Update fused with the apply,
  * 6 all Newton-Schulz products of a step in one launch (the default),
  * 7 every Newton-Schulz step of the small matrices (m <= 128, n <= 256) on chip.

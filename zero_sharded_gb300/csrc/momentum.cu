@@ -4,8 +4,10 @@
 // u is written as bf16 twice, in the tensor's rows x cols orientation and
 // transposed, because the Newton-Schulz GEMMs read X (min x max) and X^T with
 // both operands K-major; and sum(u^2) is reduced per tensor for the Frobenius
-// normalisation, deterministically (fixed shuffle tree, fixed block order, then
-// a fixed-order per-tensor sum in double), so results do not depend on timing.
+// normalisation, deterministically (fixed shuffle tree per tile, then a
+// fixed-order per-tensor sum of the tile partials in double), so results do not
+// depend on timing.  The per-tensor sum is done by whichever block finishes the
+// tensor's last tile (a per-tensor arrival counter), inside the same launch.
 //
 // HBM traffic per element: read g (4 or 2 B) and m (4 B), write m (4 B) and two
 // bf16 copies (2 + 2 B).
@@ -135,24 +137,46 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((tid & 31) == 0) warp_sum[tid >> 5] = ss;
   __syncthreads();
+  __shared__ int last;
   if (tid == 0) {
     float s = 0.f;
     for (int w = 0; w < kThreads / 32; ++w) s += warp_sum[w];
     p.partial[blockIdx.x] = s;
+    // arrival with acq_rel at GPU scope: this partial is visible before the count
+    // moves, and the last arrival sees every other tile's partial
+    int prev;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(p.tile_done + t.mat) : "memory");
+    last = prev == mm.tile_count - 1;
   }
-}
-
-// One warp per tensor: fixed-order sum of its tiles' partials in double.
-__global__ void __launch_bounds__(128) sigma_finalize_kernel(const MomParams p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= p.n_mats) return;
-  const MomMat mm = p.mats[warp];
-  double s = 0.0;
-  for (int i = lane; i < mm.tile_count; i += 32) s += (double)p.partial[mm.tile_first + i];
+  __syncthreads();
+  if (last) {
+    // every tile of the tensor has arrived (the barrier orders these reads after
+    // thread 0's acquire): sigma = 1 / (||u||_F + eps) from the tile partials,
+    // summed in double in a fixed order: thread-strided with 4 loads in flight,
+    // shuffle tree per warp, warps in index order
+    __shared__ double wsum[kThreads / 32];
+    double d = 0.0;
+    for (int i0 = tid; i0 < mm.tile_count; i0 += 4 * kThreads) {
+      float v[4];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) p.sigma[warp] = (float)(1.0 / (sqrt(s) + (double)p.eps));
+      for (int q = 0; q < 4; ++q) {
+        const int i = i0 + q * kThreads;
+        v[q] = i < mm.tile_count ? __ldcg(p.partial + mm.tile_first + i) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d += (double)v[q];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    if ((tid & 31) == 0) wsum[tid >> 5] = d;
+    __syncthreads();
+    if (tid == 0) {
+      double tot = 0.0;
+      for (int w = 0; w < kThreads / 32; ++w) tot += wsum[w];
+      p.sigma[t.mat] = (float)(1.0 / (sqrt(tot) + (double)p.eps));
+      p.tile_done[t.mat] = 0;                               // ready for the next launch
+    }
+  }
 }
 
 }  // namespace
@@ -160,14 +184,6 @@ __global__ void __launch_bounds__(128) sigma_finalize_kernel(const MomParams p) 
 cudaError_t launch_momentum(const MomParams& p, cudaStream_t s) {
   if (p.n_tiles <= 0) return cudaSuccess;
   momentum_kernel<<<p.n_tiles, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_sigma_finalize(const MomParams& p, cudaStream_t s) {
-  if (p.n_mats <= 0) return cudaSuccess;
-  const int threads = 128;
-  const int blocks = (p.n_mats * 32 + threads - 1) / threads;
-  sigma_finalize_kernel<<<blocks, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

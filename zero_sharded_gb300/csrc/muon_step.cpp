@@ -62,6 +62,7 @@ struct Layout {
   int64_t n_mom_tiles = 0;
   int64_t off_status = 0, off_sigma = 0, off_partial = 0, off_momtiles = 0, off_mommats = 0, off_matinfo = 0;
   int64_t off_small = 0;           // SmallMat per matrix of the small groups
+  int64_t off_tiledone = 0;        // momentum pass: per-tensor tile arrival counters (int32, zero)
   int32_t n_small = 0;
   int64_t off_tiles = 0;           // all GEMM tile lists
   int64_t n_gemm_tiles = 0;
@@ -145,6 +146,8 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   L.off_mommats = off; off = align_up(off + (int64_t)sizeof(MomMat) * std::max<int64_t>(n_mats, 1), kAlign);
   L.off_matinfo = off; off = align_up(off + (int64_t)sizeof(MatInfo) * std::max<int64_t>(n_mats, 1), kAlign);
   L.off_small = off;   off = align_up(off + (int64_t)sizeof(SmallMat) * std::max<int64_t>(L.n_small, 1), kAlign);
+  // inside the tables region: the zeros of the host image reset them on every call
+  L.off_tiledone = off; off = align_up(off + 4 * std::max<int64_t>(n_mats, 1), kAlign);
   // GEMM tiles: Gram + Poly (same count), and two ping-pong copies each of the
   // Update and Apply lists (a tall tensor's Apply tiles cover n x m)
   int64_t nt = 0;
@@ -468,6 +471,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   mp.n_mats = (int32_t)n_mats;
   mp.partial = reinterpret_cast<float*>(ws + L.off_partial);
   mp.sigma = reinterpret_cast<float*>(ws + L.off_sigma);
+  mp.tile_done = reinterpret_cast<int*>(ws + L.off_tiledone);
   mp.status = reinterpret_cast<int*>(ws + L.off_status);
 
   // GEMM problems
@@ -501,9 +505,8 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       for (int j = 0; j < G.count; ++j) {
         SmallMat& e = smt[n_small++];
         e.x = reinterpret_cast<const uint16_t*>(ws + G.off_x) + (int64_t)j * G.m * G.ldx;
-        e.xt = reinterpret_cast<const uint16_t*>(ws + G.off_xt[0]) + (int64_t)j * G.n * G.ldm;
         e.ldx = (int32_t)G.ldx;
-        e.ldm = (int32_t)G.ldm;
+        e.pad0 = 0;
         e.m = G.m;
         e.n = G.n;
         e.mat = G.mat_base + j;
@@ -822,7 +825,6 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
 
   const Program& P = *prog;
   if (traced(0, s, [&] { return launch_momentum(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
-  if (traced(1, s, [&] { return launch_sigma_finalize(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
   if (P.small.n_mats > 0) {
     SmallParams sp = P.small;
     sp.ns_steps = ns_steps;

@@ -2,14 +2,16 @@
 //
 // A matrix whose Newton-Schulz orientation X (m x n, m = min(rows, cols)) has
 // m <= 128 and n <= 256 is handled by one CTA from the first Gram product to the
-// apply: X, X^T, A and B' live in shared memory as K-major 128-byte-swizzled
-// bf16 operands, the three accumulators live in TMEM, and nothing but the
-// starting X / X^T (written by the momentum pass) and the parameter itself is
-// touched in global memory.  Per step (Canzona summary page, section 2, the
+// apply: X, A and B' live in shared memory as 128-byte-swizzled bf16 operands,
+// the three accumulators live in TMEM, and nothing but the starting X (written
+// by the momentum pass) and the parameter itself is touched in global memory.  Per step (Canzona summary page, section 2, the
 // Muon update with its quintic Newton-Schulz iteration):
 //   Gram    A  = s^2 X X^T                 M = 128, N = 128, K = n_pad   (TMEM cols   0..127)
 //   Poly    B' = a I + b A + c A A         M = 128, N = 128, K = 128     (TMEM cols 128..255)
-//   Update  X <- s B' X = s B' (X^T)^T     M = 128, N = n_pad, K = 128   (TMEM cols 256..)
+//   Update  X <- s B' X                    M = 128, N = n_pad, K = 128   (TMEM cols 256..)
+// X is stored once, rows of 64 consecutive columns (128 bytes): read K-major by
+// the Gram product (K = n) and MN-major by the Update (N = n, K = m), so no X^T
+// is formed.
 // with s = 1/(||u||_F + eps) in step 1 and 1 afterwards, the same folding and
 // the same bf16 rounding points as the tiled kernels.  Rows m..127 and columns
 // n..n_pad-1 are zero and stay zero (B' is a on the padded diagonal, applied to
@@ -31,16 +33,16 @@ namespace {
 
 constexpr int kSmThreads = 128;
 constexpr int kBlk = 128 * 128;                               // one 64-wide K block of 128 rows, bytes
-constexpr int kOffX = 0;                                      // X: 128 rows, K = n_pad
-constexpr int kOffXT = kOffX + (kSmallMaxN / 64) * kBlk;      // X^T: n_pad rows, K = 128
-constexpr int kOffA = kOffXT + 2 * kSmallMaxN * 128;          // A: 128 rows, K = 128
+constexpr int kOffX = 0;                                      // X: 128 rows x n_pad columns
+constexpr int kOffA = kOffX + (kSmallMaxN / 64) * kBlk;       // A: 128 rows, K = 128
 constexpr int kOffB = kOffA + 2 * kBlk;                       // B': 128 rows, K = 128
-constexpr int kOffBar = kOffB + 2 * kBlk;
+// The fp32 apply staging (m rows x (n_pad + 1) floats) reuses X, A and B' (all
+// consumed by then) and a little slack behind them.
+constexpr int kStageEnd = kSmallMaxM * (kSmallMaxN + 1) * 4;
+constexpr int kOffBar = ((kOffB + 2 * kBlk > kStageEnd ? kOffB + 2 * kBlk : kStageEnd) + 1023) & ~1023;
 constexpr int kSmallSmemBytes = 1024 /*align slack*/ + kOffBar + 64;
 constexpr uint32_t kSmallTmemCols = 512;
 constexpr int64_t kSmallDrainNs = 2000000000LL;
-// The fp32 apply staging (m rows x (n_pad + 1) floats) reuses X, X^T and A.
-static_assert(kSmallMaxM * (kSmallMaxN + 1) * 4 <= kOffB, "apply staging overlaps B'");
 static_assert(kSmallSmemBytes <= 227 * 1024, "shared memory");
 
 // Byte offset of element (row, k) in a K-major operand of `rows` rows stored as
@@ -74,7 +76,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) ns_small_kernel(const SmallPara
   }
   if (warp == 0) tmem_alloc(holder, kSmallTmemCols);
 
-  // starting X (m x n) and X^T (n x m), zero padded to 128 x n_pad and n_pad x 128;
+  // starting X (m x n), zero padded to 128 x n_pad;
   // 8 chunks per thread in flight (all loads of a batch before its smem stores)
   constexpr int kBatch = 8;
   const int xch = n_pad >> 3;
@@ -97,24 +99,6 @@ __global__ void __launch_bounds__(kSmThreads, 1) ns_small_kernel(const SmallPara
       if (i < kSmallMaxM * xch) *reinterpret_cast<uint4*>(base + kOffX + sw128(kSmallMaxM, r, k0)) = v[u];
     }
   }
-  for (int i0 = tid; i0 < n_pad * 16; i0 += kSmThreads * kBatch) {
-    uint4 v[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kSmThreads;
-      const int q = i >> 4, k0 = (i & 15) * 8;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (i < n_pad * 16 && q < n && k0 < m) {
-        v[u] = *reinterpret_cast<const uint4*>(sm.xt + (int64_t)q * sm.ldm + k0);
-        if (k0 + 8 > m) v[u] = keep_first(v[u], m - k0);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * kSmThreads;
-      if (i < n_pad * 16) *reinterpret_cast<uint4*>(base + kOffXT + sw128(n_pad, i >> 4, (i & 15) * 8)) = v[u];
-    }
-  }
   {
     // the parameter is read only by the apply at the end: bring it into L2 now
     const MatInfo& wi = p.info[sm.mat];
@@ -131,7 +115,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) ns_small_kernel(const SmallPara
   const uint32_t tmem = *holder;
   const uint32_t lrow = (uint32_t)(warp * 32) << 16;     // this warp's TMEM lane quarter
   const uint32_t tA = tmem, tP = tmem + 128, tX = tmem + 256;
-  const uint32_t sX = smem_u32(base + kOffX), sXT = smem_u32(base + kOffXT);
+  const uint32_t sX = smem_u32(base + kOffX);
   const uint32_t sA = smem_u32(base + kOffA), sB = smem_u32(base + kOffB);
   const float sg = p.sigma[sm.mat];
   const MatInfo mi = p.info[sm.mat];
@@ -210,13 +194,15 @@ __global__ void __launch_bounds__(kSmThreads, 1) ns_small_kernel(const SmallPara
     // ---------------------------------------------------------------- Update
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t id = idesc_bf16_f32(128, n_pad);
+      // B operand X, MN-major: 64-column blocks kBlk apart, 8-row groups 1024 apart;
+      // each K = 16 step takes the next 16 rows (2048 bytes)
+      const uint32_t id = idesc_bf16_f32_bmn(128, n_pad);
 #pragma unroll
       for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           umma_bf16(tX, sdesc_kmajor_sw128(sB + kb * kBlk + 32 * k),
-                    sdesc_kmajor_sw128(sXT + kb * n_pad * 128 + 32 * k), id, (kb | k) != 0);
+                    sdesc_mnmajor_sw128(sX + (kb * 4 + k) * 2048, kBlk, 1024), id, (kb | k) != 0);
       umma_commit(bar);
     }
     ok = __syncthreads_and(mbar_wait(bar, ph, nullptr, p.status, p.timeout_ns));
@@ -225,7 +211,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) ns_small_kernel(const SmallPara
     tc_fence_after();
     const float s = first ? sg : 1.f;
     if (!last) {
-      // X and X^T of the next step
+      // X of the next step
 #pragma unroll 1
       for (int j = 0; j < (n_pad >> 5); ++j) {
         float v[32];
@@ -237,10 +223,6 @@ __global__ void __launch_bounds__(kSmThreads, 1) ns_small_kernel(const SmallPara
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           *reinterpret_cast<uint4*>(base + kOffX + sw128(kSmallMaxM, tid, 32 * j + 8 * q)) = pack8(v + 8 * q);
-#pragma unroll
-        for (int q = 0; q < 32; ++q)
-          *reinterpret_cast<__nv_bfloat16*>(base + kOffXT + sw128(n_pad, 32 * j + q, tid)) =
-              __float2bfloat16_rn(v[q]);
       }
       fence_proxy_async_smem();
       tc_fence_before();

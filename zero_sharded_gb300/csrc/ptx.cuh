@@ -269,6 +269,20 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand with 128-byte swizzle:
+// rows of 128 bytes hold 64 consecutive M/N elements of one k, 8-row (8 k) swizzle
+// atoms of 1024 bytes; `lbo` = byte stride between 64-element M/N blocks, `sbo` =
+// byte stride between 8-k groups.  The base must be 1024-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);     // bits  0-13: start address >> 4
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // bits 16-29: leading byte offset >> 4
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;  // bits 32-45: stride byte offset >> 4
+  d |= (uint64_t)1u << 46;                      // bits 46-48: fixed 0b001
+  d |= (uint64_t)2u << 61;                      // bits 61-63: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                               // D format: f32
@@ -276,6 +290,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)                            // B format: bf16
          | ((uint32_t)(N >> 3) << 17)            // N >> 3
          | ((uint32_t)(M >> 4) << 24);           // M >> 4
+}
+
+// As idesc_bf16_f32 with the B operand MN-major (bit 16, "transpose B").
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one M x N x 16 step, issued by one thread.

@@ -41,11 +41,11 @@ struct MomParams {
   int32_t n_mats;
   float* partial;         // per tile: sum of u^2 over the tile
   float* sigma;           // per tensor: 1 / (||u||_F + eps)
+  int* tile_done;         // per tensor: tiles finished in this launch (zero at launch, reset by the last)
   int* status;
 };
 
 cudaError_t launch_momentum(const MomParams& p, cudaStream_t s);
-cudaError_t launch_sigma_finalize(const MomParams& p, cudaStream_t s);
 
 // ------------------------------------------------------------------ NS GEMM
 constexpr int kBM = 128;        // UMMA M (TMEM lanes)
@@ -136,15 +136,15 @@ int gemm_max_units(bool pair);   // units that can be resident at once (persiste
 
 // ------------------------------------------------------------------ small-matrix Newton-Schulz
 // Matrices with m <= kSmallMaxM and n <= kSmallMaxN run every Newton-Schulz step
-// in one CTA with X, X^T, A and B' resident in shared memory and the accumulators
+// in one CTA with X, A and B' resident in shared memory and the accumulators
 // in TMEM (one CTA per matrix, one launch for all of them).
 constexpr int kSmallMaxM = 128;
 constexpr int kSmallMaxN = 256;
 
 struct SmallMat {
   const uint16_t* x;      // bf16 X (m x n), row pitch ldx (written by the momentum pass)
-  const uint16_t* xt;     // bf16 X^T (n x m), row pitch ldm
-  int32_t ldx, ldm;
+  int32_t ldx;
+  int32_t pad0;
   int32_t m, n;
   int32_t mat;            // global matrix index (sigma, MatInfo)
   int32_t pad;
