@@ -368,7 +368,7 @@ def main():
     el = sum(r * c for r, c in my_shapes)
     # algorithmic bytes of the momentum pass: read g and m, write m and one bf16 copy of u
     mom_bytes = el * (10 + (2 if w.grad_bf16 else 4))
-    mom_moved = mom_bytes + 2 * el                             # this design also writes u^T (bf16)
+    mom_moved = mom_bytes                                      # X is written once, in its m x n orientation
     mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9 if mom_ms > 0 else 0.0
     hbm = float(peaks.get("hbm_gbs", 6800.0))
 

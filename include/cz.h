@@ -251,6 +251,12 @@ const char* cz_status_string(int status);
 /* Library version and build target, e.g. "cz 0.1 sm_103a". */
 const char* cz_version(void);
 
+/* Support (no counterpart in the paper): name and description of the CUDA error
+ * behind the most recent CZ_ERR_CUDA that a kernel launch of this thread's
+ * cz_muon_step(_ex) calls returned ("cudaSuccess: no error" if none).  The
+ * string is owned by the library and valid until the thread's next call. */
+const char* cz_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,16 +1,16 @@
 // Momentum pass of the Muon step: one streaming kernel over the owned tensors.
 //
 // Per element:  m <- mu*m + g  (fp32, stored);  u = g + mu*m  (Nesterov) or u = m;
-// u is written as bf16 twice, in the tensor's rows x cols orientation and
-// transposed, because the Newton-Schulz GEMMs read X (min x max) and X^T with
-// both operands K-major; and sum(u^2) is reduced per tensor for the Frobenius
+// u is written as bf16 in the Newton-Schulz orientation X (min x max): as is for
+// a wide tensor, transposed (through shared memory) for a tall one; and sum(u^2)
+// is reduced per tensor for the Frobenius
 // normalisation, deterministically (fixed shuffle tree per tile, then a
 // fixed-order per-tensor sum of the tile partials in double), so results do not
 // depend on timing.  The per-tensor sum is done by whichever block finishes the
 // tensor's last tile (a per-tensor arrival counter), inside the same launch.
 //
-// HBM traffic per element: read g (4 or 2 B) and m (4 B), write m (4 B) and two
-// bf16 copies (2 + 2 B).
+// HBM traffic per element: read g (4 or 2 B) and m (4 B), write m (4 B) and the
+// bf16 copy (2 B).
 
 #include <cuda_bf16.h>
 
@@ -103,8 +103,9 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
         for (int q = 0; q < n_ok; ++q) mp[q] = m[q];
       }
       // rows x cols orientation; a partial tail vector lands in the row padding
-      *reinterpret_cast<uint2*>(mm.direct + (int64_t)gr * mm.ld_direct + gc) =
-          pack_bf16x4(u[0], u[1], u[2], u[3]);
+      if (mm.direct)
+        *reinterpret_cast<uint2*>(mm.direct + (int64_t)gr * mm.ld_direct + gc) =
+            pack_bf16x4(u[0], u[1], u[2], u[3]);
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
     const int rq = cq;
     const int gc = t.c0 + c;
     const int gr = t.r0 + rq;
-    if (gc < mm.cols && gr < mm.rows) {
+    if (mm.trans && gc < mm.cols && gr < mm.rows) {
       const __nv_bfloat16* s = trT + c * kTrPitch + rq;
       __nv_bfloat162 lo = __halves2bfloat162(s[0], s[1]);
       __nv_bfloat162 hi = __halves2bfloat162(s[2], s[3]);

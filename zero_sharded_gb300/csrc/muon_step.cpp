@@ -21,6 +21,7 @@
 #include <map>
 #include <memory>
 #include <mutex>
+#include <string>
 #include <tuple>
 #include <vector>
 
@@ -50,8 +51,8 @@ struct OwnedMat {
 struct Group {
   int32_t m, n, count = 0;
   int32_t mat_base = 0;        // global matrix index of the group's first matrix
-  int64_t ldx = 0, ldm = 0;    // element pitches: X rows (n), X^T / A / B rows (m)
-  int64_t off_x = 0, off_xt[2] = {0, 0}, off_a = 0, off_b = 0;   // workspace byte offsets
+  int64_t ldx = 0, ldm = 0;    // element pitches: X rows (n), A / B' rows (m)
+  int64_t off_x[2] = {0, 0}, off_a = 0, off_b = 0;   // workspace byte offsets (X ping-pong, A, B')
   bool has_wide = false, has_tall = false;
   bool small = false;          // every Newton-Schulz step on chip (ns_small), no tiled GEMMs
 };
@@ -160,14 +161,14 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
         if (a * kBM <= b * kBN + kBN - 1) ++sym;
     const int64_t upd = ceil_div64(G.m, kBM) * ceil_div64(G.n, kBN);
     const int64_t app_t = ceil_div64(G.n, kBM) * ceil_div64(G.m, kBN);
-    nt += G.count * (2 * sym + 2 * upd + 2 * std::max(upd, app_t));
+    nt += G.count * (3 * sym + 2 * upd + 2 * std::max(upd, app_t));   // Gram x2, Poly, Update x2, Apply x2
   }
   L.n_gemm_tiles = nt;
   L.off_tiles = off; off = align_up(off + 16 * std::max<int64_t>(nt, 1), kAlign);
   // launches per step program: Gram + Poly (one per chunk of kMaxProblems groups),
   // two Update and two Apply lists (Apply: up to two problems per group)
   const int64_t G = (int64_t)L.groups.size();
-  const int64_t n_launch = 2 * ceil_div64(std::max<int64_t>(G, 1), kMaxProblems) +
+  const int64_t n_launch = 3 * ceil_div64(std::max<int64_t>(G, 1), kMaxProblems) +
                            2 * ceil_div64(std::max<int64_t>(G, 1), kMaxProblems) +
                            2 * ceil_div64(std::max<int64_t>(2 * G, 1), kMaxProblems);
   L.n_cta_entries = n_launch * (kMaxGrid + 1);
@@ -178,9 +179,10 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
     G.ldx = align_up(G.n, 8);
     G.ldm = align_up(G.m, 8);
     const int64_t c = G.count;
-    G.off_x = off;     off = align_up(off + 2 * c * G.m * G.ldx, kAlign);
-    G.off_xt[0] = off; off = align_up(off + 2 * c * G.n * G.ldm, kAlign);
-    G.off_xt[1] = off; off = align_up(off + 2 * c * G.n * G.ldm, kAlign);
+    G.off_x[0] = off;  off = align_up(off + 2 * c * G.m * G.ldx, kAlign);
+    if (!G.small) {    // the on-chip kernel keeps its iterates in shared memory
+      G.off_x[1] = off;  off = align_up(off + 2 * c * G.m * G.ldx, kAlign);
+    }
     G.off_a = off;     off = align_up(off + 2 * c * G.m * G.ldm, kAlign);
     G.off_b = off;     off = align_up(off + 2 * c * G.m * G.ldm, kAlign);
   }
@@ -250,7 +252,7 @@ bool encode_map(CUtensorMap* map, void* base, int64_t inner, int64_t rows, int64
 struct Launch {
   int phase;
   int first;
-  int cur;                          // X^T ping-pong index read by Update / Apply
+  int cur;                          // X buffer read (Gram, Update, Apply)
   GemmParams params;
 };
 
@@ -264,7 +266,7 @@ struct Program {
   std::vector<uint8_t> host_tables;   // image of [off_sigma .. off_tiles + tiles) region (tables only)
   int64_t tables_begin = 0, tables_end = 0;
   MomParams mom{};
-  std::vector<Launch> gram, poly, update[2], apply[2];
+  std::vector<Launch> gram[2], poly, update[2], apply[2];   // [cur]: X buffer read
   SmallParams small{};
 };
 
@@ -288,18 +290,26 @@ std::mutex g_prof_mu;
 bool g_prof_on = false;
 std::vector<ProfRec> g_prof;
 
+// Last CUDA error behind a CZ_ERR_CUDA of this thread (cz_last_cuda_error).
+thread_local cudaError_t t_last_cuda = cudaSuccess;
+
+cudaError_t note(cudaError_t e) {
+  if (e != cudaSuccess) t_last_cuda = e;
+  return e;
+}
+
 // Launches `fn` on stream s, bracketed by events when tracing is on.
 template <class F>
 cudaError_t traced(int kind, cudaStream_t s, F&& fn) {
-  if (!g_prof_on) return fn();
+  if (!g_prof_on) return note(fn());
   ProfRec r{kind, nullptr, nullptr};
-  if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return cudaGetLastError();
+  if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return note(cudaGetLastError());
   cudaEventRecord(r.a, s);
   cudaError_t e = fn();
   cudaEventRecord(r.b, s);
   std::lock_guard<std::mutex> lk(g_prof_mu);
   g_prof.push_back(r);
-  return e;
+  return note(e);
 }
 
 std::mutex g_mu;
@@ -427,17 +437,16 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   for (int64_t g = 0; g < n_mats; ++g) {
     const OwnedMat& om = L.mats[g];
     const Group& G = L.groups[om.group];
-    uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x) + (int64_t)om.idx * G.m * G.ldx;
-    uint16_t* XT = reinterpret_cast<uint16_t*>(ws + G.off_xt[0]) + (int64_t)om.idx * G.n * G.ldm;
+    uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x[0]) + (int64_t)om.idx * G.m * G.ldx;
     MomMat& d = mm[g];
     d.off = om.off;
     d.rows = om.rows;
     d.cols = om.cols;
-    if (!om.tall) {          // X = u (rows x cols), X^T = u^T
+    if (!om.tall) {          // X = u (rows x cols)
       d.direct = X; d.ld_direct = G.ldx;
-      d.trans = XT; d.ld_trans = G.ldm;
-    } else {                 // X = u^T, X^T = u (rows x cols)
-      d.direct = XT; d.ld_direct = G.ldm;
+      d.trans = nullptr; d.ld_trans = 0;
+    } else {                 // X = u^T
+      d.direct = nullptr; d.ld_direct = 0;
       d.trans = X; d.ld_trans = G.ldx;
     }
     d.tile_first = (int32_t)tcur;
@@ -497,14 +506,14 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   const int tm_rows = pair ? 256 : kBM;          // output rows per tile
   const uint32_t b_box = pair ? 128 : kBN;       // B-side rows each CTA loads per stage
   const int max_grid = gemm_max_units(pair);
-  std::vector<ProbDesc> gram, poly, upd[2], app[2];
+  std::vector<ProbDesc> gram[2], poly, upd[2], app[2];
   SmallMat* smt = at<SmallMat>(img, tb, L.off_small);
   int32_t n_small = 0;
   for (const Group& G : L.groups) {
     if (G.small) {
       for (int j = 0; j < G.count; ++j) {
         SmallMat& e = smt[n_small++];
-        e.x = reinterpret_cast<const uint16_t*>(ws + G.off_x) + (int64_t)j * G.m * G.ldx;
+        e.x = reinterpret_cast<const uint16_t*>(ws + G.off_x[0]) + (int64_t)j * G.m * G.ldx;
         e.ldx = (int32_t)G.ldx;
         e.pad0 = 0;
         e.m = G.m;
@@ -514,11 +523,10 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       }
       continue;
     }
-    uint16_t* X = reinterpret_cast<uint16_t*>(ws + G.off_x);
-    uint16_t* XT[2] = {reinterpret_cast<uint16_t*>(ws + G.off_xt[0]), reinterpret_cast<uint16_t*>(ws + G.off_xt[1])};
+    uint16_t* X[2] = {reinterpret_cast<uint16_t*>(ws + G.off_x[0]), reinterpret_cast<uint16_t*>(ws + G.off_x[1])};
     uint16_t* A = reinterpret_cast<uint16_t*>(ws + G.off_a);
     uint16_t* B = reinterpret_cast<uint16_t*>(ws + G.off_b);
-    const int64_t msx = (int64_t)G.m * G.ldx, mst = (int64_t)G.n * G.ldm, msa = (int64_t)G.m * G.ldm;
+    const int64_t msx = (int64_t)G.m * G.ldx, msa = (int64_t)G.m * G.ldm;
     const int c = G.count;
     // symmetric tiles of an m x m output
     std::vector<int4> sym;
@@ -526,17 +534,18 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       for (int64_t a = 0; a < ceil_div64(G.m, tm_rows); ++a)
         for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b)
           if (a * tm_rows <= b * kBN + kBN - 1) sym.push_back(make_int4(0, j, (int)a, (int)b));
-    {
-      // Gram: A = s^2 X X^T, stored with its mirror into A
+    for (int cur = 0; cur < 2; ++cur) {
+      // Gram: A = s^2 X X^T from X buffer `cur`, stored with its mirror into A
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.m; d.gp.K = G.n; d.gp.count = c; d.gp.mat_base = G.mat_base;
       d.gp.phase = kGram; d.gp.slot = 0;
-      if (!encode_map(&d.ta, X, G.n, G.m, c, G.ldx, msx, kBM) || !encode_map(&d.tb, X, G.n, G.m, c, G.ldx, msx, b_box) ||
+      if (!encode_map(&d.ta, X[cur], G.n, G.m, c, G.ldx, msx, kBM) ||
+          !encode_map(&d.tb, X[cur], G.n, G.m, c, G.ldx, msx, b_box) ||
           !encode_map(&d.to, A, G.m, G.m, c, G.ldm, msa, 0, true))
         return CZ_ERR_CUDA;
       d.tot = d.to;
       d.tiles = sym;
-      gram.push_back(d);
+      gram[cur].push_back(d);
     }
     {
       // Poly: B' = a I + b A + c A A, stored with its mirror into B
@@ -552,51 +561,26 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       poly.push_back(d);
     }
     for (int cur = 0; cur < 2; ++cur) {
-      // update: X (m x n) <- s B' X; operands B' rows (K = m) and X^T rows (K = m);
-      // stores X and X^T (into the other ping-pong buffer)
+      // update: X[cur ^ 1] (m x n) <- s B' X[cur]; operands B' rows (K = m) and
+      // X[cur] read MN-major (64 x 64 boxes: 64 columns of n, 64 rows of K = m)
       ProbDesc d{};
       d.gp.M = G.m; d.gp.N = G.n; d.gp.K = G.m; d.gp.count = c; d.gp.mat_base = G.mat_base;
       d.gp.phase = kUpdate; d.gp.slot = 2;
+      d.gp.b_mn = 1;
       if (!encode_map(&d.ta, B, G.m, G.m, c, G.ldm, msa, kBM) ||
-          !encode_map(&d.tb, XT[cur], G.m, G.n, c, G.ldm, mst, b_box) ||
-          !encode_map(&d.to, X, G.n, G.m, c, G.ldx, msx, 0, true) ||
-          !encode_map(&d.tot, XT[cur ^ 1], G.m, G.n, c, G.ldm, mst, 0, true))
+          !encode_map(&d.tb, X[cur], G.n, G.m, c, G.ldx, msx, 64) ||
+          !encode_map(&d.to, X[cur ^ 1], G.n, G.m, c, G.ldx, msx, 0, true))
         return CZ_ERR_CUDA;
-      // update tiles: B' (m x m) is the small operand, X^T (n x m) the large one
+      d.tot = d.to;
+      // update tiles: B' (m x m) is the small operand, X (m x n) the large one
       const int64_t TMu = ceil_div64(G.m, tm_rows), TNu = ceil_div64(G.n, kBN);
       const int64_t grp_u = ceil_div64(max_grid, TMu);
       for (int j = 0; j < c; ++j) grouped_tiles(d.tiles, j, TMu, TNu, true, grp_u);
       upd[cur].push_back(d);
-      // apply, wide tensors: output X (m x n) = parameter layout
-      if (G.has_wide) {
-        ProbDesc e = d;
-        e.gp.orient = 0;
-        e.gp.phase = kApply;
-        e.tiles.clear();
-        for (int j = 0; j < c; ++j) {
-          if (L.mats[G.mat_base + j].tall) continue;
-          grouped_tiles(e.tiles, j, TMu, TNu, true, grp_u);
-        }
-        app[cur].push_back(e);
-      }
-      // apply, tall tensors: output X^T (n x m) = parameter layout; operands X^T rows and B rows
-      if (G.has_tall) {
-        ProbDesc e{};
-        e.gp.M = G.n; e.gp.N = G.m; e.gp.K = G.m; e.gp.count = c; e.gp.mat_base = G.mat_base;
-        e.gp.orient = 1;
-        e.gp.phase = kApply; e.gp.slot = 2;
-        if (!encode_map(&e.ta, XT[cur], G.m, G.n, c, G.ldm, mst, kBM) ||
-            !encode_map(&e.tb, B, G.m, G.m, c, G.ldm, msa, b_box))
-          return CZ_ERR_CUDA;
-        // X^T (n x m, A side) is the large operand, B' (m x m, B side) the small one
-        const int64_t TMt = ceil_div64(G.n, tm_rows), TNt = ceil_div64(G.m, kBN);
-        const int64_t grp_t = ceil_div64(max_grid, TNt);
-        for (int j = 0; j < c; ++j) {
-          if (!L.mats[G.mat_base + j].tall) continue;
-          grouped_tiles(e.tiles, j, TMt, TNt, false, grp_t);
-        }
-        app[cur].push_back(e);
-      }
+      // apply: the same product, the epilogue writes W (X for a wide tensor, X^T for a tall one)
+      ProbDesc e = d;
+      e.gp.phase = kApply;
+      app[cur].push_back(e);
     }
   }
   // Gram with first=0/1 share one tile list: build first, copy for the other flag.
@@ -604,7 +588,8 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     make_launches(phase, probs, dev_tiles, host_tiles, cursor, dev_cta, host_cta, cta_cursor, max_grid, common, out,
                   0, cur);
   };
-  ml(kGram, gram, P.gram, 0);
+  ml(kGram, gram[0], P.gram[0], 0);
+  ml(kGram, gram[1], P.gram[1], 1);
   ml(kPoly, poly, P.poly, 0);
   for (int cur = 0; cur < 2; ++cur) {
     ml(kUpdate, upd[cur], P.update[cur], cur);
@@ -631,16 +616,16 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   // expected arrivals per (matrix, slot): tiles of the matrix x epilogue warps per unit
   const int arrivals = kEpiWarps * (pair ? 2 : 1);
   int32_t* expect = at<int32_t>(img, tb, L.off_expect);
-  for (auto& pd : gram)
+  for (auto& pd : gram[0])
     for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 0] += arrivals;
   for (auto& pd : poly)
     for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 1] += arrivals;
   for (auto& pd : upd[0])
     for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 2] += arrivals;
 
-  // fused launch: one problem table over the six lists, each list walked per unit
-  const std::vector<Launch>* lists[kFusedLists] = {&P.gram, &P.poly, &P.update[0], &P.update[1], &P.apply[0],
-                                                   &P.apply[1]};
+  // fused launch: one problem table over the seven lists, each list walked per unit
+  const std::vector<Launch>* lists[kFusedLists] = {&P.gram[0], &P.gram[1], &P.poly,     &P.update[0],
+                                                   &P.update[1], &P.apply[0], &P.apply[1]};
   bool ok_fused = true;
   int total = 0;
   for (auto* v : lists) {
@@ -843,7 +828,7 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
   for (int t = 0; t < ns_steps; ++t) {
     const int first = t == 0 ? 1 : 0;
     const int cur = t & 1;
-    for (const Launch& ln : P.gram) {
+    for (const Launch& ln : P.gram[cur]) {
       gp = ln.params;
       gp.first = first;
       if (traced(2, s, [&] { return launch_ns_gemm(kGram, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
@@ -931,5 +916,11 @@ const char* cz_status_string(int status) {
 }
 
 const char* cz_version(void) { return "cz 0.1 sm_103a"; }
+
+const char* cz_last_cuda_error(void) {
+  thread_local std::string msg;
+  msg = std::string(cudaGetErrorName(t_last_cuda)) + ": " + cudaGetErrorString(t_last_cuda);
+  return msg.c_str();
+}
 
 }  // extern "C"

@@ -3,14 +3,15 @@
 // One kernel template, one launch per Newton-Schulz product, grouped over every
 // owned tensor of the shard (tensors of the same shape form one batched
 // "problem"; a launch carries up to kMaxProblems of them and a flat tile list).
-// All products are D = A * B^T with both operands K-major bf16 and an fp32
-// accumulator in TMEM:
-//   Gram    A  = X X^T                  operands X rows, X rows      (K = n)
+// All products are D = A * B^T with bf16 operands and an fp32 accumulator in TMEM:
+//   Gram    A  = X X^T                  operands X rows, X rows      (K = n, both K-major)
 //   Poly    B' = a I + b A + c A A^T    operands A rows, A rows      (K = m), A symmetric
-//   Update  X <- B' X = B' (X^T)^T      operands B' rows, X^T rows   (K = m)
+//   Update  X' <- B' X                  operands B' rows (K-major), X (MN-major: K = m
+//                                       rows of n contiguous columns)
 // a X + B X = (a I + B) X, so the a X term rides in the Poly output and the
-// Update epilogue reads no operand.  The Update also writes X^T for the next
-// step, so no MN-major operand is needed.  Step 1 folds the Frobenius
+// Update epilogue reads no operand.  X is kept only in its m x n orientation, in
+// two buffers: the Update reads one and writes the other (tiles of one column
+// block read every row of X).  Step 1 folds the Frobenius
 // normalisation in as scalars: A_1 = s^2 X~X~^T and X_1 = s B'_1 X~,
 // s = 1/(||u||_F + eps).  The last Update instead runs the apply epilogue:
 // W <- W - lr*sqrt(max(1,rows/cols)) * X_K in fp32, the bf16 parameter copy,
@@ -106,6 +107,11 @@ struct Pre {
   float4 w[8];    // 32 fp32 master weights (Apply)
 };
 
+// Component c of v, c known at compile time after unrolling (keeps Pre in registers).
+__device__ __forceinline__ float& f4(float4& v, int c) {
+  return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+}
+
 template <int PHASE>
 __device__ __forceinline__ void prefetch(Pre& pre, const GemmParams& p, const GemmProblem& pr, int mat,
                                          const MatInfo& mi, int rbase, int lane, int col0) {
@@ -120,6 +126,16 @@ __device__ __forceinline__ void prefetch(Pre& pre, const GemmParams& p, const Ge
                                                       : make_uint4(0u, 0u, 0u, 0u);
   }
   if constexpr (PHASE == kApply) {
+    if (mi.rows > mi.cols) {
+      // tall W = X^T: this lane's D row is W column rbase + lane; entry q holds W row col0 + q
+      const int i = rbase + lane;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int j = col0 + q;
+        f4(pre.w[q >> 2], q & 3) = (i < pr.M && j < pr.N) ? p.W[mi.w_off + (int64_t)j * mi.cols + i] : 0.f;
+      }
+      return;
+    }
     // W in the coalesced layout of apply_chunk: entry 4h+i holds row rbase + 8i + lane/4,
     // columns col0 + 16h + 4(lane%4) .. +3
     if (mi.vec_ok) {
@@ -154,12 +170,31 @@ __device__ __forceinline__ void stage_block(__nv_bfloat16* D, __nv_bfloat16* T, 
 // updated and written with lanes across columns: each instruction touches 8 rows
 // x 64 contiguous bytes instead of 32 rows x 16 bytes.  W was prefetched in the
 // same layout (prefetch<kApply>).  In the parameter's rows x cols layout:
-// W <- W - delta, bf16 copy = RNE(W), optional debug delta.
+// W <- W - delta, bf16 copy = RNE(W), optional debug delta.  A tall parameter
+// holds X^T: its chunk is written column by column straight from the lanes.
 constexpr int kApplyPitch = 20;   // floats per staged row (16 + 4): conflict-free v4 writes
 
 __device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProblem& pr, const MatInfo& mi, int rbase,
-                                            int col0, const float* v, const Pre& pre, float* stage, int lane) {
+                                            int col0, const float* v, Pre& pre, float* stage, int lane) {
   const float lrs = mi.lrs;
+  if (mi.rows > mi.cols) {
+    // tall W (n x m) = X^T: D element (row i, column j) is W[j][i]; the lanes (rows i)
+    // cover 32 consecutive W columns, so each column q of the chunk is one 128-byte access
+    const int i = rbase + lane;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      const int j = col0 + q;
+      if (i < pr.M && j < pr.N) {
+        const float d = lrs * v[q];
+        const int64_t idx = mi.w_off + (int64_t)j * mi.cols + i;
+        const float w = f4(pre.w[q >> 2], q & 3) - d;
+        p.W[idx] = w;
+        if (p.Wb) reinterpret_cast<__nv_bfloat16*>(p.Wb)[idx] = __float2bfloat16_rn(w);
+        if (p.dbg) p.dbg[idx] = d;
+      }
+    }
+    return;
+  }
   const bool vec = mi.vec_ok != 0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -215,7 +250,7 @@ struct Walker {
   bool open = false;
   __device__ Walker(const GemmParams& p_, int unit_) : p(p_), unit(unit_) {}
   __device__ int list_of(int i, int sl) const {
-    return sl == 0 ? 0 : sl == 1 ? 1 : (i + 1 == p.ns_steps ? 4 : 2) + (i & 1);
+    return sl == 0 ? (i & 1) : sl == 1 ? 2 : (i + 1 == p.ns_steps ? 5 : 3) + (i & 1);
   }
   // Next tile: its entry, global problem index, Newton-Schulz step and slot.
   __device__ bool next(int4& tl, int& prob, int& iter, int& sl) {
@@ -255,6 +290,15 @@ struct Walker {
     }
   }
 };
+
+// Whether a tile's B operand is read MN-major: fixed by the phase where it can be
+// (Gram and Poly never, Update and Apply always), else per problem.
+template <int PHASE>
+__device__ __forceinline__ bool b_operand_mn(const GemmProblem& pr) {
+  if constexpr (PHASE == kGram || PHASE == kPoly) return false;
+  else if constexpr (PHASE == kUpdate || PHASE == kApply) return true;
+  else return pr.b_mn != 0;
+}
 
 // Completion counter and arrivals of the stage a fused tile depends on
 // (previous slot of the same Newton-Schulz step, or the last slot of the step before).
@@ -357,7 +401,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, co
 #pragma unroll
         for (int q = 0; q < 32; ++q) v[q] *= s;   // Gram: s = sigma^2; Update: s = sigma (step 1)
       }
-      const bool do_t = !kSym || rbase < col0;
+      const bool do_t = kSym && rbase < col0;     // the mirror of a block above the diagonal
       if (lane == 0 && e.pending) bulk_wait_read_all();
       __syncwarp();
       stage_block(e.stD, e.stT, v, lane, do_t);
@@ -375,6 +419,8 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, co
   return true;
 }
 
+// 10 warps: two of the four SM sub-partitions hold 3 warps, so a thread gets at
+// most 16384 / 96 registers (168 after rounding).
 template <int PHASE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<PAIR>;
@@ -418,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         tma_prefetch_desc(&p.tmB[i]);
         if (PHASE != kApply && p.prob[i].phase != kApply) {   // Apply problems store no tiles
           tma_prefetch_desc(&p.tmO[i]);
-          tma_prefetch_desc(&p.tmOT[i]);
+          if (p.prob[i].phase != kUpdate) tma_prefetch_desc(&p.tmOT[i]);
         }
       }
     }
@@ -451,16 +497,28 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           if (w) {
             uint8_t* da = sm.a + stage * C::kBytesA;
             uint8_t* db = sm.b + stage * C::kBytesB;
+            // A: one box of its rows x 64 k; B the same when K-major, else 64 x 64 boxes
+            // (64 N columns x 64 k rows, 8 KB each) side by side
             if constexpr (PAIR) {
               // both CTAs' copies complete on the even CTA's full barrier
               const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), 0);
               if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * C::kStageBytes);
               tma_load_3d_pair(da, ma, fb, kb * kBK, arow, tl.y);
-              tma_load_3d_pair(db, mb, fb, kb * kBK, brow, tl.y);
+              if (b_operand_mn<PHASE>(pr)) {
+                for (int j = 0; j < C::kRowsB / 64; ++j)
+                  tma_load_3d_pair(db + j * 8192, mb, fb, brow + 64 * j, kb * kBK, tl.y);
+              } else {
+                tma_load_3d_pair(db, mb, fb, kb * kBK, brow, tl.y);
+              }
             } else {
               mbar_arrive_expect_tx(&sm.full[stage], C::kStageBytes);
               tma_load_3d(da, ma, &sm.full[stage], kb * kBK, arow, tl.y);
-              tma_load_3d(db, mb, &sm.full[stage], kb * kBK, brow, tl.y);
+              if (b_operand_mn<PHASE>(pr)) {
+                for (int j = 0; j < C::kRowsB / 64; ++j)
+                  tma_load_3d(db + j * 8192, mb, &sm.full[stage], brow + 64 * j, kb * kBK, tl.y);
+              } else {
+                tma_load_3d(db, mb, &sm.full[stage], kb * kBK, brow, tl.y);
+              }
             }
             issued |= 1u << stage;
             last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -487,14 +545,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (even CTA only)
     if (rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(C::kTileM, kBN);
+      constexpr uint32_t idesc_kk = idesc_bf16_f32(C::kTileM, kBN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       Walker<PHASE> walk(p, unit);
       int4 tl;
       int prob, iter, sl;
       while (ok && walk.next(tl, prob, iter, sl)) {
-        const int nk = ceil_div(p.prob[prob].K, kBK);
+        const GemmProblem& pr = p.prob[prob];
+        const int nk = ceil_div(pr.K, kBK);
+        const bool b_mn = b_operand_mn<PHASE>(pr);
+        // MN-major B: bit 16 of the instruction descriptor
+        const uint32_t idesc = idesc_kk | (b_mn ? (1u << 16) : 0u);
+        // descriptors of stage 0, K step 0; a stage adds its byte offset, a K = 16 step
+        // adds 32 bytes (K-major) or 16 rows = 2048 bytes (MN-major; boxes 8192 apart),
+        // all in the 16-byte units of the start-address field (addresses < 256 KB: no carry)
+        const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(sm.a));
+        const uint64_t db0 = b_mn ? sdesc_mnmajor_sw128(smem_u32(sm.b), 8192, 1024) : sdesc_kmajor_sw128(smem_u32(sm.b));
+        const uint32_t a_step = 32 / 16, b_step = b_mn ? 2048 / 16 : 32 / 16;
         bool w = true;
         if (lane == 0) w = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort, p.status, p.timeout_ns);
         if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
@@ -508,11 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           }
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t a0 = smem_u32(sm.a + stage * C::kBytesA);
-            const uint32_t b0 = smem_u32(sm.b + stage * C::kBytesB);
+            const uint64_t as = da0 + stage * (uint32_t)(C::kBytesA / 16);
+            const uint64_t bs = db0 + stage * (uint32_t)(C::kBytesB / 16);
 #pragma unroll
             for (int s = 0; s < kBK / 16; ++s) {
-              const uint64_t ad = sdesc_kmajor_sw128(a0 + s * 32), bd = sdesc_kmajor_sw128(b0 + s * 32);
+              const uint64_t ad = as + s * a_step, bd = bs + s * b_step;
               if constexpr (PAIR) umma_bf16_pair(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
               else umma_bf16(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
             }

@@ -20,8 +20,8 @@ struct MomTile {
 struct MomMat {
   int64_t off;            // element offset of the tensor in the flat buffers
   int32_t rows, cols;     // parameter layout (rows x cols, row-major)
-  uint16_t* direct;       // bf16 buffer receiving u in rows x cols orientation
-  uint16_t* trans;        // bf16 buffer receiving u^T (cols x rows)
+  uint16_t* direct;       // bf16 buffer receiving u in rows x cols orientation, or null
+  uint16_t* trans;        // bf16 buffer receiving u^T (cols x rows), or null
   int64_t ld_direct;      // element pitch of `direct` rows
   int64_t ld_trans;       // element pitch of `trans` rows
   int32_t tile_first;     // first tile of this tensor (its partial sums are contiguous)
@@ -58,18 +58,22 @@ constexpr int kMaxGrid = 1024;  // upper bound on the persistent grid (SM count)
 enum Phase : int32_t {
   kGram = 0,     // A = s^2 X X^T                   (symmetric output)
   kPoly = 1,     // B' = a I + b A + c A A          (symmetric output)
-  kUpdate = 2,   // X <- s B' X, also writes X^T     (= s (a X + B X))
-  kApply = 3,    // last step: W <- W - lr*scale*s B' X  (+ bf16 copy, debug delta)
+  kUpdate = 2,   // X' <- s B' X into the other X buffer (= s (a X + B X))
+  kApply = 3,    // last step: W <- W - lr*scale*s B' X, transposed for a tall W (+ bf16 copy, debug delta)
   kFused = 4,    // every product of all ns_steps in one launch, per-matrix dependencies
 };
 
 // One batched GEMM: `count` matrices of the same M x N x K, operands read by
-// the two tensor maps of the same index (A side: M rows, B side: N rows, both
-// K-major), output written by the epilogue of the launch's phase.
+// the two tensor maps of the same index (A side: M rows, B side: N rows), output
+// written by the epilogue of the launch's phase.  The A operand is K-major (rows of
+// K elements, 64 x 128-row boxes); the B operand too (64 x 128- or 256-row boxes)
+// unless b_mn is set: then it is stored with N contiguous (X, read by the Update
+// and the Apply) and loaded as 64 (N) x 64 (K) boxes.
 struct GemmProblem {
   int32_t M, N, K, count;
+  int32_t b_mn;           // B operand read MN-major
+  int32_t pad;
   int32_t mat_base;       // global index (sigma / MatInfo) of matrix 0 of this problem
-  int32_t orient;         // kApply: 0 -> output is X (m x n), 1 -> output is X^T (n x m)
   int32_t phase;          // kGram .. kApply (read by the fused launch)
   int32_t slot;           // position in a Newton-Schulz step: 0 Gram, 1 Poly, 2 Update/Apply
   const uint16_t* aux;   int64_t ld_aux, ms_aux;     // kPoly: A (for the b A term)
@@ -90,13 +94,13 @@ struct TileList {
   int32_t prob_off;           // the list's problem 0 in GemmParams::prob
   int32_t pad;
 };
-constexpr int kFusedLists = 6;  // Gram, Poly, Update (X^T buffer 0), Update (1), Apply (0), Apply (1)
+constexpr int kFusedLists = 7;  // Gram (X buffer 0), Gram (1), Poly, Update (0), Update (1), Apply (0), Apply (1)
 
 struct GemmParams {
-  CUtensorMap tmA[kMaxProblems];    // A-side operand loads (128 x 64 boxes, 128-byte swizzle)
-  CUtensorMap tmB[kMaxProblems];    // B-side operand loads (256 x 64 boxes)
-  CUtensorMap tmO[kMaxProblems];    // output stores, 32 x 32 boxes (Gram/Poly: A or B'; Update: X)
-  CUtensorMap tmOT[kMaxProblems];   // transposed-output stores (Gram/Poly: same matrix; Update: X^T)
+  CUtensorMap tmA[kMaxProblems];    // A-side operand loads (128-byte swizzle)
+  CUtensorMap tmB[kMaxProblems];    // B-side operand loads
+  CUtensorMap tmO[kMaxProblems];    // output stores, 32 x 32 boxes (Gram/Poly: A or B'; Update: X')
+  CUtensorMap tmOT[kMaxProblems];   // mirrored-output stores of the symmetric products (same matrix)
   GemmProblem prob[kMaxProblems];
   int32_t n_prob;
   int32_t n_tiles;

@@ -44,8 +44,8 @@ class cz_step_opts(ctypes.Structure):
 
 
 class CzError(RuntimeError):
-    def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} failed: {status} ({cz_status_string(status)})")
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        super().__init__(f"{fn} failed: {status} ({cz_status_string(status)})" + (f": {detail}" if detail else ""))
         self.status = status
 
 
@@ -104,6 +104,7 @@ def load() -> ctypes.CDLL:
                                             ctypes.c_void_p, ctypes.c_void_p]),
         "cz_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "cz_version": (ctypes.c_char_p, []),
+        "cz_last_cuda_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -136,6 +137,8 @@ def _stream_ptr(stream) -> Optional[int]:
 
 def _check(fn: str, st: int):
     if st != CZ_OK:
+        if st == CZ_ERR_CUDA:
+            raise CzError(fn, st, load().cz_last_cuda_error().decode())
         raise CzError(fn, st)
 
 
@@ -145,6 +148,10 @@ def cz_status_string(status: int) -> str:
 
 def cz_version() -> str:
     return load().cz_version().decode()
+
+
+def cz_last_cuda_error() -> str:
+    return load().cz_last_cuda_error().decode()
 
 
 def cz_make_buckets(numels: Sequence[int], cap_elems: int) -> List[int]:
