@@ -85,7 +85,11 @@ def ns_flops_executed(shapes, steps=NS_STEPS, bm=128, bn=256):
 # under profiles/, keyed by a hash of the kernel sources they were taken with: once any source changes the
 # figure no longer describes the kernel and the bench reports null.
 NCU_TRAFFIC = {
-    "4d8f1a72aa913e54": {"qwen3-1.7b-layer": {"ns_update": 303.57e6, "momentum": 748.31e6}},
+    "0baead91a18c3800": {
+        "qwen3-1.7b-layer": {"ns_fused": 2772.49e6, "momentum": 649.21e6, "ns_gram": 127.50e6, "ns_poly": 51.79e6,
+                             "ns_update": 217.87e6, "ns_update_apply": 609.63e6},
+        "tiny": {"ns_small": 0.3425e6},
+    },
 }
 
 
@@ -475,6 +479,8 @@ def main():
             "momentum_pass": {"bound": "hbm", "achieved": mom_gbs, "peak": hbm, "unit": "GB/s",
                               "frac": mom_gbs / hbm if hbm else None, "bytes_per_element": mom_bytes / max(el, 1),
                               "moved_bytes_per_element": mom_moved / max(el, 1),
+                              "traffic": NCU_TRAFFIC.get(kernel_source_hash(), {}).get(w.name, {}).get("momentum")
+                              if world == 1 else None,
                               "ms_per_step": mom_ms, "peak_source": f"hbm_gbs of {peak_src}"},
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
             "cpu_baseline": cpu, "e2e": e2e,
