@@ -60,9 +60,12 @@ def ns_flops_by_kind(shapes, steps=NS_STEPS):
             "ns_fused": steps * (2 * g + p), "ns_small": steps * (2 * gs + ps)}
 
 
-def ns_flops_executed(shapes, steps=NS_STEPS, bm=128, bn=256):
-    """Flops the tensor cores execute: 128x256 tiles, symmetric products on upper tiles only;
-    on-chip small matrices as 128-row products with n padded to 64."""
+def ns_flops_executed(shapes, steps=NS_STEPS, bn=256):
+    """Flops the tensor cores execute: 256x256 tiles on CTA pairs (128x256 with CZ_NS_PAIR=0), symmetric
+    products on the tiles touching the upper triangle only; on-chip small matrices as 128-row products
+    with n padded to 64."""
+    bm = 128 if os.environ.get("CZ_NS_PAIR", "1") == "0" else 256
+
     def cdiv(a, b):
         return (a + b - 1) // b
     tot = 0
@@ -376,32 +379,56 @@ def main():
     mom_gbs = mom_bytes / (mom_ms * 1e-3) / 1e9 if mom_ms > 0 else 0.0
     hbm = float(peaks.get("hbm_gbs", 6800.0))
 
-    # ---------------- end to end: host gradients in, bf16 parameters out, every step
+    # ---------------- end to end: host gradients in, bf16 parameters out, every step.
+    # Every step copies its fp32 (or bf16) gradients from pinned host memory and reads its bf16 parameters
+    # back; the copies run on two copy streams and overlap the neighbouring steps' compute (device gradient
+    # and bf16-parameter buffers are double-buffered; momentum and the fp32 master are shared, so steps stay
+    # ordered). Inputs (201 MB of gradients, 201 MB master, 201 MB momentum on the default layer) exceed the
+    # L2, so no flush is inserted. Value = (end of the last read-back - start of the first copy) / K.
     e2e = None
     if not args.no_e2e:
         Gh = G.to("cpu").pin_memory()
-        PBh = torch.empty(PB.shape, dtype=PB.dtype).pin_memory()
-        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup + args.steps):
-                flush.zero_()
-                j = i - args.warmup
-                if j >= 0:
-                    es[j].record(stream)
-                G.copy_(Gh, non_blocking=True)
-                step()
-                PBh.copy_(PB, non_blocking=True)
-                if j >= 0:
-                    ee[j].record(stream)
+        PBh = [torch.empty(PB.shape, dtype=PB.dtype).pin_memory() for _ in range(2)]
+        Gd = [G, torch.empty_like(G)]
+        PBd = [PB, torch.empty_like(PB)]
+        optsd = [cz.make_opts(param_bf16=PBd[i], workspace=WS, workspace_bytes=ws_bytes, grad_is_bf16=w.grad_bf16)
+                 for i in range(2)]
+        h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        n = args.warmup + args.steps
+        ev_h2d = [torch.cuda.Event() for _ in range(n)]
+        ev_step = [torch.cuda.Event() for _ in range(n)]
+        ev_d2h = [torch.cuda.Event() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        e_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(es, ee))
+        for i in range(n):
+            b = i & 1
+            if i == args.warmup:
+                torch.cuda.synchronize()
+                t0.record(h2d)
+            with torch.cuda.stream(h2d):
+                if i >= 2:
+                    h2d.wait_event(ev_step[i - 2])             # the device buffer's previous user is done
+                Gd[b].copy_(Gh, non_blocking=True)
+                ev_h2d[i].record(h2d)
+            stream.wait_event(ev_h2d[i])
+            if i >= 2:
+                stream.wait_event(ev_d2h[i - 2])             # bf16 buffer read back before it is rewritten
+            cz.cz_muon_step_ex(plan, my_rank, P, Gd[b], M, sargs, LR, MU, NS_STEPS, stream, optsd[b])
+            ev_step[i].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev_step[i])
+                PBh[b].copy_(PBd[b], non_blocking=True)
+                ev_d2h[i].record(d2h)
+        t1.record(d2h)
+        torch.cuda.synchronize()
+        e_ms = t0.elapsed_time(t1) / args.steps
         te = torch.tensor([e_ms], device=dev)
         if world > 1:
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
         e2e = {"value": float(te.item()) / world, "unit": "ms",
                "h2d_bytes_per_step": int(G.numel() * G.element_size()),
-               "d2h_bytes_per_step": int(PB.numel() * PB.element_size())}
+               "d2h_bytes_per_step": int(PB.numel() * PB.element_size()),
+               "overlap": "two copy streams; step j+1's gradient copy and step j's read-back overlap compute"}
 
     # roofline of the dominant kernel (largest share of the step's device time)
     dom = max(prof, key=lambda k: prof[k][0])
