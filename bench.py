@@ -509,6 +509,9 @@ def main():
                               "traffic": NCU_TRAFFIC.get(kernel_source_hash(), {}).get(w.name, {}).get("momentum")
                               if world == 1 else None,
                               "ms_per_step": mom_ms, "peak_source": f"hbm_gbs of {peak_src}"},
+            "step_ms_stats": {"median": statistics.median(step_ms),
+                              "p90": sorted(step_ms)[min(len(step_ms) - 1, int(round(0.9 * (len(step_ms) - 1))))],
+                              "min": min(step_ms), "max": max(step_ms), "rank": rank},
             "kernels_ms_per_step": {k: v[0] / args.steps for k, v in prof.items()},
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)),
