@@ -696,24 +696,31 @@ cudaError_t launch_phase(const GemmParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
+  // The fused launch's units wait on one another's completion counters, so it is a
+  // cooperative launch: the runtime guarantees that every CTA is resident at once
+  // (or refuses the launch) even when other work shares the GPU.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((PAIR ? 2 : 1) * p.grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int n_attr = 0;
   if constexpr (PAIR) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * p.grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kGemmSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<PHASE, PAIR>, p);
-  } else {
-    ns_gemm_kernel<PHASE, PAIR><<<p.grid, kThreads, kGemmSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
   }
+  if constexpr (PHASE == kFused) {
+    attr[n_attr].id = cudaLaunchAttributeCooperative;
+    attr[n_attr].val.cooperative = 1;
+    ++n_attr;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n_attr;
+  return cudaLaunchKernelEx(&cfg, ns_gemm_kernel<PHASE, PAIR>, p);
 }
 
 }  // namespace
