@@ -369,6 +369,22 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, co
   if constexpr (PH == kApply) mi = p.mats[gm];
   Pre cur;
   const int first_c = need ? __ffs(need) - 1 : 0;
+  if constexpr (PH == kApply) {
+    // the master weights of this warp's whole share of the tile into L2 while the MMAs run:
+    // 32 D rows x 128 D columns = 128 lines of 128 bytes, 4 per lane
+    if (need) {
+      const bool tall = mi.rows > mi.cols;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int line = lane * 4 + q;                // 0..127
+        int wr, wc;                                   // W row and first W column of the line
+        if (tall) { wr = col_first + line; wc = rbase; }                        // W rows = D columns
+        else { wr = rbase + (line >> 2); wc = col_first + (line & 3) * 32; }    // 4 lines per D row
+        if (wr < mi.rows && wc < mi.cols)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(p.W + mi.w_off + (int64_t)wr * mi.cols + wc));
+      }
+    }
+  }
   if (need) prefetch<PH>(cur, p, pr, mat, mi, rbase, lane, col_first + first_c * 32);
   const bool w = mbar_wait(&e.tfull[acc], acc_phase, e.abort, p.status, p.timeout_ns);
   if (!__all_sync(0xffffffffu, w)) return false;
