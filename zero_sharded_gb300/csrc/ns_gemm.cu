@@ -560,7 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer (even CTA only)
-    if (rank == 0) {
+    // One thread runs the whole issue loop: tcgen05.mma is single-thread, and keeping
+    // the other lanes out removes a warp shuffle and a warp barrier from every k-block.
+    if (rank == 0 && lane == 0) {
       constexpr uint32_t idesc_kk = idesc_bf16_f32(C::kTileM, kBN);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
@@ -579,53 +581,42 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
         const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(sm.a));
         const uint64_t db0 = b_mn ? sdesc_mnmajor_sw128(smem_u32(sm.b), 8192, 1024) : sdesc_kmajor_sw128(smem_u32(sm.b));
         const uint32_t a_step = 32 / 16, b_step = b_mn ? 2048 / 16 : 32 / 16;
-        bool w = true;
-        if (lane == 0) w = mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort, p.status, p.timeout_ns);
-        if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
+        if (!mbar_wait(&sm.tempty[acc], acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + acc * (uint32_t)kBN;
         for (int kb = 0; kb < nk; ++kb) {
-          if (lane == 0) w = mbar_wait(&sm.full[stage], phase, abort, p.status, p.timeout_ns);
-          if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
+          if (!mbar_wait(&sm.full[stage], phase, abort, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (lane == 0) {
-            const uint64_t as = da0 + stage * (uint32_t)(C::kBytesA / 16);
-            const uint64_t bs = db0 + stage * (uint32_t)(C::kBytesB / 16);
+          const uint64_t as = da0 + stage * (uint32_t)(C::kBytesA / 16);
+          const uint64_t bs = db0 + stage * (uint32_t)(C::kBytesB / 16);
 #pragma unroll
-            for (int s = 0; s < kBK / 16; ++s) {
-              const uint64_t ad = as + s * a_step, bd = bs + s * b_step;
-              if constexpr (PAIR) umma_bf16_pair(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
-              else umma_bf16(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
-            }
-            if constexpr (PAIR) umma_commit_pair(&sm.empty[stage], 0x3);   // frees the stage in both CTAs
-            else umma_commit(&sm.empty[stage]);
+          for (int s = 0; s < kBK / 16; ++s) {
+            const uint64_t ad = as + s * a_step, bd = bs + s * b_step;
+            if constexpr (PAIR) umma_bf16_pair(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
+            else umma_bf16(d, ad, bd, idesc, (kb | s) != 0 ? 1u : 0u);
           }
-          __syncwarp();
+          if constexpr (PAIR) umma_commit_pair(&sm.empty[stage], 0x3);   // frees the stage in both CTAs
+          else umma_commit(&sm.empty[stage]);
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          if constexpr (PAIR) umma_commit_pair(&sm.tfull[acc], 0x3);     // both halves of the accumulator
-          else umma_commit(&sm.tfull[acc]);
-        }
-        __syncwarp();
+        if constexpr (PAIR) umma_commit_pair(&sm.tfull[acc], 0x3);     // both halves of the accumulator
+        else umma_commit(&sm.tfull[acc]);
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // wait until every issued MMA has completed (TMEM is released below)
-      if (lane == 0) {
-        if constexpr (PAIR) umma_commit_pair(sm.drain, 0x1);
-        else umma_commit(sm.drain);
-        mbar_wait(sm.drain, 0, nullptr, p.status, kDrainTimeoutNs);
-      }
-      __syncwarp();
+      if constexpr (PAIR) umma_commit_pair(sm.drain, 0x1);
+      else umma_commit(sm.drain);
+      mbar_wait(sm.drain, 0, nullptr, p.status, kDrainTimeoutNs);
     }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue (both CTAs of a pair)
     const int ew = warp - 2;                    // 0 .. kEpiWarps-1
