@@ -474,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer (both CTAs of a pair)
+    // One thread runs the whole loop (TMA copies are single-thread instructions).
     if (lane == 0) {
       for (int i = 0; i < p.n_prob; ++i) {
         tma_prefetch_desc(&p.tmA[i]);
@@ -483,79 +484,71 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           if (p.prob[i].phase != kUpdate) tma_prefetch_desc(&p.tmOT[i]);
         }
       }
-    }
-    uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;   // bit s: parity of stage s's last fill
-    bool ok = true;
-    Walker<PHASE> walk(p, unit);
-    int4 tl;
-    int prob, iter, sl;
-    while (ok && walk.next(tl, prob, iter, sl)) {
-      const GemmProblem& pr = p.prob[prob];
-      if constexpr (PHASE == kFused) {
-        // the matrix's previous stage must be complete (and visible) before its data is loaded
-        const int* ctr;
-        int target;
-        if (fused_dependency(p, pr.mat_base + tl.y, iter, sl, &ctr, &target)) {
-          bool w = true;
-          if (lane == 0) w = counter_wait(ctr, target, abort, p.status, p.timeout_ns);
-          if (!__shfl_sync(0xffffffffu, (int)w, 0)) break;
+      uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;   // bit s: parity of stage s's last fill
+      bool ok = true;
+      Walker<PHASE> walk(p, unit);
+      int4 tl;
+      int prob, iter, sl;
+      while (ok && walk.next(tl, prob, iter, sl)) {
+        const GemmProblem& pr = p.prob[prob];
+        if constexpr (PHASE == kFused) {
+          // the matrix's previous stage must be complete (and visible) before its data is loaded
+          const int* ctr;
+          int target;
+          if (fused_dependency(p, pr.mat_base + tl.y, iter, sl, &ctr, &target) &&
+              !counter_wait(ctr, target, abort, p.status, p.timeout_ns))
+            break;
         }
-      }
-      const int nk = ceil_div(pr.K, kBK);
-      const CUtensorMap* ma = &p.tmA[prob];
-      const CUtensorMap* mb = &p.tmB[prob];
-      const int arow = tl.z * C::kTileM + (int)rank * 128;
-      const int brow = tl.w * kBN + (int)rank * C::kRowsB;
-      for (int kb = 0; kb < nk; ++kb) {
-        bool w = true;
-        if (lane == 0) {
-          w = mbar_wait(&sm.empty[stage], phase ^ 1u, abort, p.status, p.timeout_ns);
-          if (w) {
-            uint8_t* da = sm.a + stage * C::kBytesA;
-            uint8_t* db = sm.b + stage * C::kBytesB;
-            // A: one box of its rows x 64 k; B the same when K-major, else 64 x 64 boxes
-            // (64 N columns x 64 k rows, 8 KB each) side by side
-            if constexpr (PAIR) {
-              // both CTAs' copies complete on the even CTA's full barrier
-              const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), 0);
-              if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * C::kStageBytes);
-              tma_load_3d_pair(da, ma, fb, kb * kBK, arow, tl.y);
-              if (b_operand_mn<PHASE>(pr)) {
-                for (int j = 0; j < C::kRowsB / 64; ++j)
-                  tma_load_3d_pair(db + j * 8192, mb, fb, brow + 64 * j, kb * kBK, tl.y);
-              } else {
-                tma_load_3d_pair(db, mb, fb, kb * kBK, brow, tl.y);
-              }
+        const int nk = ceil_div(pr.K, kBK);
+        const CUtensorMap* ma = &p.tmA[prob];
+        const CUtensorMap* mb = &p.tmB[prob];
+        const int arow = tl.z * C::kTileM + (int)rank * 128;
+        const int brow = tl.w * kBN + (int)rank * C::kRowsB;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          uint8_t* da = sm.a + stage * C::kBytesA;
+          uint8_t* db = sm.b + stage * C::kBytesB;
+          // A: one box of its rows x 64 k; B the same when K-major, else 64 x 64 boxes
+          // (64 N columns x 64 k rows, 8 KB each) side by side
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on the even CTA's full barrier
+            const uint32_t fb = mapa_shared(smem_u32(&sm.full[stage]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&sm.full[stage], 2 * C::kStageBytes);
+            tma_load_3d_pair(da, ma, fb, kb * kBK, arow, tl.y);
+            if (b_operand_mn<PHASE>(pr)) {
+              for (int j = 0; j < C::kRowsB / 64; ++j)
+                tma_load_3d_pair(db + j * 8192, mb, fb, brow + 64 * j, kb * kBK, tl.y);
             } else {
-              mbar_arrive_expect_tx(&sm.full[stage], C::kStageBytes);
-              tma_load_3d(da, ma, &sm.full[stage], kb * kBK, arow, tl.y);
-              if (b_operand_mn<PHASE>(pr)) {
-                for (int j = 0; j < C::kRowsB / 64; ++j)
-                  tma_load_3d(db + j * 8192, mb, &sm.full[stage], brow + 64 * j, kb * kBK, tl.y);
-              } else {
-                tma_load_3d(db, mb, &sm.full[stage], kb * kBK, brow, tl.y);
-              }
+              tma_load_3d_pair(db, mb, fb, kb * kBK, brow, tl.y);
             }
-            issued |= 1u << stage;
-            last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          } else {
+            mbar_arrive_expect_tx(&sm.full[stage], C::kStageBytes);
+            tma_load_3d(da, ma, &sm.full[stage], kb * kBK, arow, tl.y);
+            if (b_operand_mn<PHASE>(pr)) {
+              for (int j = 0; j < C::kRowsB / 64; ++j)
+                tma_load_3d(db + j * 8192, mb, &sm.full[stage], brow + 64 * j, kb * kBK, tl.y);
+            } else {
+              tma_load_3d(db, mb, &sm.full[stage], kb * kBK, brow, tl.y);
+            }
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
-        if (!__shfl_sync(0xffffffffu, (int)w, 0)) {
-          ok = false;
-          break;
-        }
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
       }
-    }
-    // every issued copy must land before the CTA may exit; a pair's copies are
-    // counted on the even CTA's barriers, and the odd CTA waits for the even one
-    // at the final cluster barrier
-    if (lane == 0 && rank == 0) {
-      for (int s = 0; s < C::kStages; ++s)
-        if (issued & (1u << s)) mbar_wait(&sm.full[s], (last_par >> s) & 1u, nullptr, p.status, kDrainTimeoutNs);
+      // every issued copy must land before the CTA may exit; a pair's copies are
+      // counted on the even CTA's barriers, and the odd CTA waits for the even one
+      // at the final cluster barrier
+      if (rank == 0) {
+        for (int s = 0; s < C::kStages; ++s)
+          if (issued & (1u << s)) mbar_wait(&sm.full[s], (last_par >> s) & 1u, nullptr, p.status, kDrainTimeoutNs);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
