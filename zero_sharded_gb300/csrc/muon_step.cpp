@@ -614,7 +614,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   if (cursor > L.n_gemm_tiles || cta_cursor > L.n_cta_entries) return CZ_ERR_NOMEM;
 
   // expected arrivals per (matrix, slot): tiles of the matrix x epilogue warps per unit
-  const int arrivals = kEpiWarps * (pair ? 2 : 1);
+  const int arrivals = kFusedEpiWarps * (pair ? 2 : 1);
   int32_t* expect = at<int32_t>(img, tb, L.off_expect);
   for (auto& pd : gram[0])
     for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 0] += arrivals;

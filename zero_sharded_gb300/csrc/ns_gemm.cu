@@ -42,7 +42,8 @@ namespace cz {
 
 namespace {
 
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Threads of a launch of phase P: producer warp, MMA warp, epilogue warps.
+__host__ __device__ constexpr int threads_of(int phase) { return 64 + 32 * epi_warps(phase); }
 // Limit of the drain waits at exit (in-flight TMA copies and MMAs must finish
 // before shared memory and TMEM are released); independent of p.timeout_ns.
 constexpr int64_t kDrainTimeoutNs = 2000000000LL;
@@ -331,7 +332,7 @@ struct EpiCtx {
 // directly and mirrored, a diagonal block directly, a block below not at all (its
 // mirror comes from the block above), so each element is written exactly once.
 // Returns false if the wait for the accumulator ran out.
-template <int PH, bool PAIR>
+template <int PH, bool PAIR, int EW>
 __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, const GemmProblem& pr, int prob,
                                               int mat, int tile_m, int tile_n, bool first, uint32_t acc,
                                               uint32_t acc_phase) {
@@ -340,7 +341,8 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, co
   const int lane = e.lane;
   const int gm = pr.mat_base + mat;
   const int rbase = tile_m * C::kTileM + (int)e.rank * 128 + e.quad * 32;
-  const int ch_first = e.half * 4;
+  constexpr int kChunks = 32 / EW;            // 32-column chunks per warp (the lane quarter's 8, shared by EW/4 warps)
+  const int ch_first = e.half * kChunks;
   const int col_first = tile_n * kBN + ch_first * 32;
   auto release = [&]() {
     tc_fence_before();
@@ -354,7 +356,7 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, co
   uint32_t need = 0;
   if (rbase < pr.M) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < kChunks; ++c) {
       const int col0 = col_first + c * 32;
       if (col0 < pr.N && (!kSym || rbase <= col0)) need |= 1u << c;
     }
@@ -371,15 +373,14 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, co
   const int first_c = need ? __ffs(need) - 1 : 0;
   if constexpr (PH == kApply) {
     // the master weights of this warp's whole share of the tile into L2 while the MMAs run:
-    // 32 D rows x 128 D columns = 128 lines of 128 bytes, 4 per lane
+    // 32 D rows x (32 kChunks) D columns = 32 kChunks lines of 128 bytes, kChunks per lane
     if (need) {
       const bool tall = mi.rows > mi.cols;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int line = lane * 4 + q;                // 0..127
+      for (int q = 0; q < kChunks; ++q) {
         int wr, wc;                                   // W row and first W column of the line
-        if (tall) { wr = col_first + line; wc = rbase; }                        // W rows = D columns
-        else { wr = rbase + (line >> 2); wc = col_first + (line & 3) * 32; }    // 4 lines per D row
+        if (tall) { wr = col_first + lane * kChunks + q; wc = rbase; }   // W rows = D columns
+        else { wr = rbase + lane; wc = col_first + q * 32; }             // kChunks lines per D row
         if (wr < mi.rows && wc < mi.cols)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(p.W + mi.w_off + (int64_t)wr * mi.cols + wc));
       }
@@ -435,10 +436,12 @@ __device__ __forceinline__ bool epilogue_tile(const GemmParams& p, EpiCtx& e, co
   return true;
 }
 
-// 10 warps: two of the four SM sub-partitions hold 3 warps, so a thread gets at
-// most 16384 / 96 registers (168 after rounding).
+// Per-product launches run 10 warps: two of the four SM sub-partitions hold 3 warps,
+// so a thread gets at most 16384 / 96 registers (168 after rounding).  The fused
+// launch runs 6 warps (at most 2 per sub-partition: up to 255 registers).
 template <int PHASE, bool PAIR>
-__global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int EW = epi_warps(PHASE);
   using C = Cfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   Smem sm = carve<PAIR>(smem_raw);
@@ -455,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tfull[i], 1);
-      mbar_init(&sm.tempty[i], kEpiWarps * (PAIR ? 2 : 1));   // one arrival per epilogue warp
+      mbar_init(&sm.tempty[i], EW * (PAIR ? 2 : 1));   // one arrival per epilogue warp
     }
     mbar_init(sm.drain, 1);
     *sm.abort = 0;
@@ -612,14 +615,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue (both CTAs of a pair)
-    const int ew = warp - 2;                    // 0 .. kEpiWarps-1
+    const int ew = warp - 2;                    // 0 .. EW-1
     EpiCtx e;
     e.tfull = sm.tfull;
     e.tempty = sm.tempty;
     e.abort = abort;
     e.tmem_base = tmem_base;
     e.quad = warp & 3;                          // TMEM lane quarter this warp may access
-    e.half = ew >> 2;                           // which 128 of the 256 accumulator columns
+    e.half = ew >> 2;                           // which share of the 256 accumulator columns
     e.lane = lane;
     e.rank = rank;
     e.lane_field = (uint32_t)(e.quad * 32) << 16;
@@ -636,20 +639,20 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
       if constexpr (PHASE == kFused) {
         const bool first = iter == 0;
         switch (pr.phase) {
-          case kGram: ok = epilogue_tile<kGram, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase); break;
+          case kGram: ok = epilogue_tile<kGram, PAIR, EW>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase); break;
           case kPoly: {
             // the Poly epilogue reads A directly: acquire the Gram stage it depends on
             const int* ctr;
             int target;
             if (fused_dependency(p, pr.mat_base + tl.y, iter, sl, &ctr, &target))
               counter_wait(ctr, target, abort, p.status, p.timeout_ns);
-            ok = epilogue_tile<kPoly, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase);
+            ok = epilogue_tile<kPoly, PAIR, EW>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase);
             break;
           }
           case kUpdate:
-            ok = epilogue_tile<kUpdate, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase);
+            ok = epilogue_tile<kUpdate, PAIR, EW>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase);
             break;
-          default: ok = epilogue_tile<kApply, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase); break;
+          default: ok = epilogue_tile<kApply, PAIR, EW>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase); break;
         }
         // publish this warp's part of the tile once its stores are complete; the
         // last step's Apply has no successor
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_kernel(const __grid_const
           __syncwarp();
         }
       } else {
-        ok = epilogue_tile<PHASE, PAIR>(p, e, pr, prob, tl.y, tl.z, tl.w, p.first != 0, acc, acc_phase);
+        ok = epilogue_tile<PHASE, PAIR, EW>(p, e, pr, prob, tl.y, tl.z, tl.w, p.first != 0, acc, acc_phase);
       }
       if (!ok) break;
       acc ^= 1u;
@@ -701,7 +704,7 @@ cudaError_t launch_phase(const GemmParams& p, cudaStream_t s) {
   // (or refuses the launch) even when other work shares the GPU.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((PAIR ? 2 : 1) * p.grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of(PHASE), 1, 1);
   cfg.dynamicSmemBytes = kGemmSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -753,7 +756,7 @@ int gemm_max_units(bool pair) {
     return sms / 2 > 0 ? sms / 2 : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2 > 0 ? sms / 2 : 1), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of(kUpdate), 1, 1);
   cfg.dynamicSmemBytes = kGemmSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -125,7 +125,13 @@ struct GemmParams {
 };
 
 // Dynamic shared memory of the GEMM kernel.
-constexpr int kEpiWarps = 8;                                  // two per TMEM lane quarter
+// Epilogue warps: two per TMEM lane quarter for the one-product launches (the apply's
+// master-weight traffic wants the memory parallelism), one per quarter for the fused
+// launch (fewer warps competing with the producer and MMA threads for issue slots;
+// measured faster there, slower for the per-product Poly and Apply).
+constexpr int kEpiWarps = 8;                                  // the most any variant uses (shared memory)
+constexpr int kFusedEpiWarps = 4;
+__host__ __device__ constexpr int epi_warps(int phase) { return phase == kFused ? kFusedEpiWarps : kEpiWarps; }
 constexpr int kStageBytesA = kBM * kBK * 2;
 constexpr int kStageBytesB = kBN * kBK * 2;
 constexpr int kEpiBlockBytes = 32 * 32 * 2;                   // one dense 32 x 32 bf16 block
