@@ -822,8 +822,14 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
       return CZ_ERR_CUDA;
     gp = P.fused;
     gp.ns_steps = ns_steps;
-    if (traced(6, s, [&] { return launch_ns_gemm(kFused, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
-    return CZ_OK;
+    const cudaError_t e = traced(6, s, [&] { return launch_ns_gemm(kFused, P.pair, gp, s); });
+    if (e == cudaSuccess) return CZ_OK;
+    // The runtime refused the launch (e.g. it cannot guarantee that all units are
+    // resident at once): clear the error and run one launch per product instead.
+    if (e != cudaErrorCooperativeLaunchTooLarge && e != cudaErrorLaunchOutOfResources &&
+        e != cudaErrorNotSupported && e != cudaErrorInvalidConfiguration)
+      return CZ_ERR_CUDA;
+    cudaGetLastError();
   }
   for (int t = 0; t < ns_steps; ++t) {
     const int first = t == 0 ? 1 : 0;

@@ -35,6 +35,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "ptx.cuh"
 #include "step_kernels.h"
 
@@ -687,6 +689,17 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
   }
 }
 
+// CZ_NS_COOPERATIVE=0 launches the fused kernel without the cooperative attribute,
+// for tools that cannot replay a cooperative cluster launch; its units are then
+// co-resident only because the grid is the occupancy limit.
+bool cooperative_fused() {
+  static const bool on = [] {
+    const char* e = std::getenv("CZ_NS_COOPERATIVE");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 template <int PHASE, bool PAIR>
 cudaError_t launch_phase(const GemmParams& p, cudaStream_t s) {
   static int configured_device = -1;
@@ -717,9 +730,11 @@ cudaError_t launch_phase(const GemmParams& p, cudaStream_t s) {
     ++n_attr;
   }
   if constexpr (PHASE == kFused) {
-    attr[n_attr].id = cudaLaunchAttributeCooperative;
-    attr[n_attr].val.cooperative = 1;
-    ++n_attr;
+    if (cooperative_fused()) {
+      attr[n_attr].id = cudaLaunchAttributeCooperative;
+      attr[n_attr].val.cooperative = 1;
+      ++n_attr;
+    }
   }
   cfg.attrs = attr;
   cfg.numAttrs = n_attr;
