@@ -262,6 +262,10 @@ def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
     assert off["launches"]["ns_fused"] == 0 and off["launches"]["ns_gram"] >= 10  # >= one Gram launch per step
     assert torch.equal(on["P"], off["P"])
     assert torch.equal(on["M"], off["M"])
+    # the same launch without the cooperative attribute (the form profilers replay)
+    plain = _run_child(tmp_path, "CZ_NS_COOPERATIVE", "0", shapes)
+    assert plain["launches"]["ns_fused"] == 2
+    assert torch.equal(on["P"], plain["P"])
 
 
 SMALL_SHAPES = [(1, 5), (7, 1), (3, 256), (256, 128), (128, 256), (100, 130), (130, 100), (64, 64),
