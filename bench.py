@@ -474,6 +474,29 @@ def main():
                  "unpack_gbs": 2 * el_all * esz / (unpack_ms * 1e-3) / 1e9}
     del padded
 
+    # standalone scale-and-apply (the apply the step fuses into its last Newton-Schulz epilogue) on the
+    # shard's tensors: reads W and U (fp32), writes W and the bf16 copy; L2 flushed before each launch
+    my_offs = [o for o, ow in zip(w.offsets, owner) if ow == my_rank]
+    U = torch.empty_like(P).normal_(generator=torch.Generator(device=dev).manual_seed(7))
+    n_ap = max(3, min(args.steps, 10))
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_ap)]
+    with torch.cuda.stream(stream):
+        cz.cz_apply_update(P, PB, U, my_offs, my_shapes, 1e-6, True, stream)
+        for i in range(n_ap):
+            flush.zero_()
+            ev_a[2 * i].record(stream)
+            cz.cz_apply_update(P, PB, U, my_offs, my_shapes, 1e-6, True, stream)
+            ev_a[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    ap_ms = statistics.mean(ev_a[2 * i].elapsed_time(ev_a[2 * i + 1]) for i in range(n_ap))
+    ap_bytes = el * 14
+    apply_standalone = {"bound": "hbm", "kernel": "apply_kernel", "achieved": ap_bytes / (ap_ms * 1e-3) / 1e9,
+                        "peak": hbm, "unit": "GB/s", "frac": ap_bytes / (ap_ms * 1e-3) / 1e9 / hbm,
+                        "bytes_per_element": 14, "launch_ms": ap_ms, "launches_timed": n_ap,
+                        "traffic": NCU_TRAFFIC.get(kernel_source_hash(), {}).get(w.name, {}).get("apply")
+                        if world == 1 else None, "peak_source": f"hbm_gbs of {peak_src}"}
+    del U
+
     # planner timing on the 64-layer Qwen3-32B layout (host work, as the pages' "milliseconds" claim)
     full = wl.qwen3_32b_reverse()
     fb = cz.cz_make_buckets(full.numels, full.bucket_cap)
@@ -516,7 +539,7 @@ def main():
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clk, "wall_s_timed_region": wall,
-            "planner": planner, "comm_pack": comm_pack,
+            "planner": planner, "comm_pack": comm_pack, "apply_standalone": apply_standalone,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

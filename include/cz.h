@@ -141,6 +141,30 @@ int cz_bucket_pack(const void* bucket, int32_t elem_bytes, const int64_t* elem_c
 int cz_bucket_unpack(const void* padded, int32_t elem_bytes, const int64_t* elem_cuts, int32_t R,
                      int64_t block, void* bucket, void* stream);
 
+/* Standalone scale-and-apply of updates already in the parameters' layout: the
+ * apply the Muon step fuses into its last Newton-Schulz epilogue, as a kernel of
+ * its own.  Section 3.4 of the summary page gives the rule
+ * W_{t+1} = W_t - eta * MatrixOp(W_t, grad W_t) ("The Atomicity Constraint ...")
+ * and, as stage 4 of the TP micro-group lifecycle ("The TP Task Abstraction"),
+ * the element-wise local add of received update shards, P_local += Delta W_local
+ * (lr = -1, shape_scale = 0).
+ *   flat_param:  fp32 device buffer (4-byte aligned), updated in place;
+ *   param_bf16:  nullable bf16 device copy in the same flat layout, written as
+ *                RNE(new fp32 value);
+ *   flat_update: fp32 device buffer U in the same flat layout (tensor i at
+ *                [offsets[i], offsets[i] + rows*cols), row-major rows x cols);
+ *   offsets:     n_tensors host int64; shapes: 2*n_tensors host int64 (rows, cols).
+ * Per tensor: coef = fp32(lr * sqrt(max(1, rows/cols))) (coef = fp32(lr) when
+ * shape_scale = 0), then W <- fp32(W - fp32(coef * U)) element by element (two
+ * roundings, the same arithmetic as the fused apply).  Bytes outside the listed
+ * tensors are not touched.  Overlapping tensors, non-positive shapes, negative
+ * offsets, a non-finite lr or shape_scale not 0/1 give CZ_ERR_INVALID before any
+ * launch; n_tensors = 0 is a no-op.  Asynchronous on `stream`; requires an
+ * sm_103a device (CZ_ERR_UNSUPPORTED otherwise). */
+int cz_apply_update(float* flat_param, void* param_bf16, const float* flat_update,
+                    const int64_t* offsets, const int64_t* shapes, int64_t n_tensors,
+                    float lr, int32_t shape_scale, void* stream);
+
 /* Options of the Muon step.  Fill with cz_step_opts_default, then override. */
 typedef struct {
   int32_t nesterov;        /* 1: u = g + mu*m (default); 0: u = m                       */

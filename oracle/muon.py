@@ -98,6 +98,18 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def apply_update(W: np.ndarray, X: np.ndarray, lr: float, shape_scale_on: bool = True) -> np.ndarray:
+    """Step 5 alone: fp32(W - lr * sqrt(max(1, rows/cols)) * X), computed in fp64 and rounded once.
+
+    W is the fp32 rows x cols tensor, X the update in the same layout; with
+    shape_scale_on False the coefficient is lr alone (the TP lifecycle's local
+    add P += Delta W is lr = -1)."""
+    W = np.asarray(W, dtype=np.float32)
+    rows, cols = W.shape
+    coef = lr * (shape_scale(rows, cols) if shape_scale_on else 1.0)
+    return (W.astype(np.float64) - coef * np.asarray(X, dtype=np.float64)).astype(np.float32)
+
+
 def muon_step_tensor(W: np.ndarray, g: np.ndarray, m: np.ndarray, lr: float, mu: float,
                      steps: int = 5, coeffs=QUINTIC, eps: float = EPS):
     """One Muon step on one whole tensor (rows x cols).
@@ -110,7 +122,7 @@ def muon_step_tensor(W: np.ndarray, g: np.ndarray, m: np.ndarray, lr: float, mu:
     m_new, u = momentum(g, m, mu)
     X = orthogonalise(u, steps, coeffs, eps)
     delta = lr * shape_scale(rows, cols) * X
-    W_new = (W.astype(np.float64) - delta).astype(np.float32)
+    W_new = apply_update(W, X, lr)
     return W_new, m_new, bf16_rne(W_new), delta
 
 

@@ -204,3 +204,25 @@ def test_bf16_storage_alone_can_exceed_the_update_bar():
     e1 = np.linalg.norm(orthogonalise_bf16(u, 1) - M.orthogonalise(u, 1)) / np.linalg.norm(M.orthogonalise(u, 1))
     assert e1 < 1e-2
     assert e5 > 1.5e-2
+
+
+def test_apply_update_hand_worked_values():
+    """Step 5 on dyadic values (exact in fp32 and fp64): tall 8 x 2 has scale 2, wide 2 x 8 scale 1."""
+    W = np.full((8, 2), 1.0, np.float32)
+    X = np.full((8, 2), 0.5)
+    assert np.array_equal(M.apply_update(W, X, 0.25), np.full((8, 2), 0.75, np.float32))      # 1 - 0.25*2*0.5
+    Wt = np.full((2, 8), 1.0, np.float32)
+    assert np.array_equal(M.apply_update(Wt, X.T, 0.25), np.full((2, 8), 0.875, np.float32))  # 1 - 0.25*0.5
+    # no shape scale, lr = -1: the TP local add P + Delta W
+    assert np.array_equal(M.apply_update(W, X, -1.0, False), np.full((8, 2), 1.5, np.float32))
+    # X = 0 leaves W unchanged
+    Wr = np.random.default_rng(0).standard_normal((5, 3)).astype(np.float32)
+    assert np.array_equal(M.apply_update(Wr, np.zeros((5, 3)), 0.02), Wr)
+
+
+def test_apply_update_rounds_once():
+    """The fp64 result is rounded to fp32 once: 1 - 2^-25 is a tie between 1 - 2^-24 and 1
+    (goes to 1, even mantissa); 1 - 3*2^-26 is nearer to 1 - 2^-24."""
+    one = np.ones((1, 1), np.float32)
+    assert M.apply_update(one, np.full((1, 1), 2.0 ** -25), 1.0, False)[0, 0] == np.float32(1.0)
+    assert M.apply_update(one, np.full((1, 1), 3 * 2.0 ** -26), 1.0, False)[0, 0] == np.float32(1.0 - 2.0 ** -24)

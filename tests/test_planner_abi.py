@@ -135,3 +135,23 @@ def test_workspace_size_grows_with_shard():
     approx = sum(4 * r * c + 4 * min(r, c) ** 2 for r, c in w.shapes)
     assert approx <= s1 <= approx * 1.05
     assert s2 >= s1 * 0.95
+
+
+def test_apply_validation_before_any_gpu_work():
+    """cz_apply_update rejects bad arguments on the host; an empty list is a no-op."""
+    fake = 0x1000
+    cz.cz_apply_update(None, None, None, [], [], 0.02)          # n_tensors = 0: nothing to do
+    cases = [
+        dict(offsets=[0, 10], shapes=[(4, 4), (2, 2)]),          # overlapping tensors
+        dict(offsets=[-4], shapes=[(2, 2)]),                     # negative offset
+        dict(offsets=[0], shapes=[(0, 3)]),                      # empty shape
+        dict(offsets=[0], shapes=[(2, 2)], lr=math.inf),         # non-finite lr
+        dict(offsets=[0], shapes=[(2, 2)], param=None),          # missing buffer
+        dict(offsets=[0], shapes=[(2, 2)], param=fake + 2),      # fp32 buffer not 4-byte aligned
+    ]
+    for cse in cases:
+        with pytest.raises(cz.CzError) as e:
+            cz.cz_apply_update(cse.get("param", fake), None, fake, cse["offsets"], cse["shapes"], cse.get("lr", 0.02))
+        assert e.value.status == cz.CZ_ERR_INVALID, cse
+    st = cz.load().cz_apply_update(fake, None, fake, cz._i64([0]), cz._i64([2, 2]), 1, 0.02, 2, None)
+    assert st == cz.CZ_ERR_INVALID                               # shape_scale must be 0 or 1

@@ -188,9 +188,9 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProbl
     for (int q = 0; q < 32; ++q) {
       const int j = col0 + q;
       if (i < pr.M && j < pr.N) {
-        const float d = lrs * v[q];
+        const float d = __fmul_rn(lrs, v[q]);   // two roundings, as the wide path (no contraction)
         const int64_t idx = mi.w_off + (int64_t)j * mi.cols + i;
-        const float w = f4(pre.w[q >> 2], q & 3) - d;
+        const float w = __fsub_rn(f4(pre.w[q >> 2], q & 3), d);
         p.W[idx] = w;
         if (p.Wb) reinterpret_cast<__nv_bfloat16*>(p.Wb)[idx] = __float2bfloat16_rn(w);
         if (p.dbg) p.dbg[idx] = d;

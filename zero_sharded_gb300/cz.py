@@ -102,6 +102,8 @@ def load() -> ctypes.CDLL:
                                           ctypes.c_void_p, ctypes.c_void_p]),
         "cz_bucket_unpack": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, _i64p, ctypes.c_int32, ctypes.c_int64,
                                             ctypes.c_void_p, ctypes.c_void_p]),
+        "cz_apply_update": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, _i64p, _i64p,
+                                           ctypes.c_int64, ctypes.c_float, ctypes.c_int32, ctypes.c_void_p]),
         "cz_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "cz_version": (ctypes.c_char_p, []),
         "cz_last_cuda_error": (ctypes.c_char_p, []),
@@ -366,3 +368,11 @@ def cz_bucket_unpack(padded, elem_cuts: Sequence[int], block: int, bucket, strea
     R = len(elem_cuts) - 1
     _check("cz_bucket_unpack", load().cz_bucket_unpack(_ptr(padded), int(padded.element_size()), _i64(elem_cuts), R,
                                                        int(block), _ptr(bucket), _stream_ptr(stream)))
+
+
+def cz_apply_update(flat_param, param_bf16, flat_update, offsets: Sequence[int], shapes: Sequence[Tuple[int, int]],
+                    lr: float, shape_scale: bool = True, stream=None) -> None:
+    """W <- W - fp32(lr * sqrt(max(1, rows/cols))) * U per listed tensor (bf16 copy optional)."""
+    _check("cz_apply_update", load().cz_apply_update(_ptr(flat_param), _ptr(param_bf16), _ptr(flat_update),
+                                                     _i64(offsets), _shapes_flat(shapes), len(offsets), float(lr),
+                                                     1 if shape_scale else 0, _stream_ptr(stream)))
