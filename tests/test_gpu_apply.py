@@ -92,6 +92,14 @@ def test_apply_without_bf16_copy():
     _check(W, U, offs, shapes, Wg, None, 0.5)
 
 
+def test_apply_more_tensors_than_one_launch_takes():
+    """300 small tensors (one launch takes 256): the second launch covers the rest; ragged gaps between."""
+    shapes = [(3 + (i % 5), 2 + (i % 7)) for i in range(300)]
+    gaps = [i % 3 for i in range(300)]
+    W, U, offs, Wg, PB = _run_apply(shapes, gaps, lr=0.02, seed=5)
+    _check(W, U, offs, shapes, Wg, PB, 0.02)
+
+
 def test_apply_full_qwen3_1p7b_layer():
     w = wl.qwen3_1p7b_layers(1)
     W, U, offs, Wg, PB = _run_apply(w.shapes, [0] * len(w.shapes), lr=0.02, seed=3)

@@ -129,6 +129,20 @@ __device__ __forceinline__ void prefetch(Pre& pre, const GemmParams& p, const Ge
                                                       : make_uint4(0u, 0u, 0u, 0u);
   }
   if constexpr (PHASE == kApply) {
+    if (mi.rows > mi.cols && mi.vec_ok) {
+      // tall W = X^T, in the coalesced layout of apply_chunk: entry 4h+k holds W row col0 + 8k + lane/4
+      // (D column), W columns rbase + 16h + 4(lane%4) .. +3 (D rows)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = col0 + 8 * k + (lane >> 2);
+          const int c = rbase + 16 * h + 4 * (lane & 3);
+          if (j < pr.N && c < pr.M)
+            pre.w[4 * h + k] = *reinterpret_cast<const float4*>(p.W + mi.w_off + (int64_t)j * mi.cols + c);
+        }
+      return;
+    }
     if (mi.rows > mi.cols) {
       // tall W = X^T: this lane's D row is W column rbase + lane; entry q holds W row col0 + q
       const int i = rbase + lane;
@@ -174,12 +188,44 @@ __device__ __forceinline__ void stage_block(__nv_bfloat16* D, __nv_bfloat16* T, 
 // x 64 contiguous bytes instead of 32 rows x 16 bytes.  W was prefetched in the
 // same layout (prefetch<kApply>).  In the parameter's rows x cols layout:
 // W <- W - delta, bf16 copy = RNE(W), optional debug delta.  A tall parameter
-// holds X^T: its chunk is written column by column straight from the lanes.
+// holds X^T: its chunk goes through smem transposed, so W is again updated with
+// lanes across its columns (or, when W rows are not 16-byte aligned, written
+// column by column straight from the lanes).
 constexpr int kApplyPitch = 20;   // floats per staged row (16 + 4): conflict-free v4 writes
 
 __device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProblem& pr, const MatInfo& mi, int rbase,
                                             int col0, const float* v, Pre& pre, float* stage, int lane) {
   const float lrs = mi.lrs;
+  if (mi.rows > mi.cols && mi.vec_ok) {
+    // tall W = X^T with 16-byte W access: the chunk's delta goes through smem transposed (W row jj =
+    // D column, 32 floats per row; 4-float groups XOR-swizzled by the row's parity, so both the
+    // column writes and the float4 row reads are free of bank conflicts), then W is updated with
+    // lanes across its columns in the layout prefetch<kApply> loaded
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < 32; ++q)
+      stage[q * 32 + ((((lane >> 2) ^ ((q & 1) << 2)) << 2) | (lane & 3))] = __fmul_rn(lrs, v[q]);
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int jj = 8 * k + (lane >> 2);
+        const int g4 = 4 * h + (lane & 3);
+        const int j = col0 + jj, c = rbase + 4 * g4;
+        if (j >= pr.N || c >= pr.M) continue;   // cols % 4 == 0: the 4 columns are in range together
+        const float4 d = *reinterpret_cast<const float4*>(stage + jj * 32 + ((g4 ^ ((jj & 1) << 2)) << 2));
+        const int64_t idx = mi.w_off + (int64_t)j * mi.cols + c;
+        float4 w = pre.w[4 * h + k];
+        w.x = __fsub_rn(w.x, d.x); w.y = __fsub_rn(w.y, d.y); w.z = __fsub_rn(w.z, d.z); w.w = __fsub_rn(w.w, d.w);
+        *reinterpret_cast<float4*>(p.W + idx) = w;
+        if (p.Wb)
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.Wb) + idx) =
+              make_uint2(pack_bf16x2(w.x, w.y), pack_bf16x2(w.z, w.w));
+        if (p.dbg) *reinterpret_cast<float4*>(p.dbg + idx) = d;
+      }
+    return;
+  }
   if (mi.rows > mi.cols) {
     // tall W (n x m) = X^T: D element (row i, column j) is W[j][i]; the lanes (rows i)
     // cover 32 consecutive W columns, so each column q of the chunk is one 128-byte access
