@@ -98,8 +98,8 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("19fe2944970da155", {"qwen3-1.7b-layer": {"ns_fused": 2627.11e6, "ns_gram": 125.54e6, "ns_poly": 50.91e6,
-                                                    "ns_update": 216.89e6, "ns_update_apply": 615.70e6}}),
+    "ns_gemm": ("72a9886e993a32e9", {"qwen3-1.7b-layer": {"ns_fused": 2640.89e6, "ns_gram": 125.27e6, "ns_poly": 51.42e6,
+                                                    "ns_update": 217.37e6, "ns_update_apply": 618.62e6}}),
     "momentum": ("b50806fa6e626836", {"qwen3-1.7b-layer": {"momentum": 649.31e6}}),
     "ns_small": ("4a183756f9b748ce", {"tiny": {"ns_small": 0.3425e6}}),
     "apply": ("789ff539365bfd36", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
