@@ -192,7 +192,9 @@ int cz_workspace_size(const cz_plan* plan, int32_t rank, const int64_t* shapes, 
 /* One Muon step over the tensors that `plan` assigns to `rank`
  * (section 3.4, "Runtime Static-Layout Enforcement", phase 2).
  *   flat_param: fp32 master weights, flat_grad: fp32 (or bf16, see opts),
- *   flat_mom: fp32 momentum -- device buffers in one flat layout; parameter p
+ *   flat_mom: fp32 momentum -- device buffers in one flat layout, each 16-byte
+ *   aligned (a bf16 gradient, the bf16 parameter copy: 8-byte aligned; the
+ *   debug output: 16-byte aligned; CZ_ERR_INVALID otherwise); parameter p
  *   occupies [offsets[p], offsets[p] + rows*cols) row-major (rows x cols = out x in).
  *   offsets: n_params host int64; shapes: 2*n_params host int64.
  *   Only tensors with owner == rank are read or written; every other byte of

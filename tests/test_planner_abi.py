@@ -123,6 +123,17 @@ def test_step_validation_before_any_gpu_work():
     with pytest.raises(cz.CzError) as e:
         cz.cz_muon_step(p, 0, None, fake, fake, args, 0.02, 0.95, 5)
     assert e.value.status == cz.CZ_ERR_INVALID
+    # base addresses must allow 16-byte vectors (a view at an odd element offset is refused, not run)
+    for bad in ((fake + 4, fake, fake), (fake, fake + 8, fake), (fake, fake, fake + 4)):
+        with pytest.raises(cz.CzError) as e:
+            cz.cz_muon_step(p, 0, *bad, args, 0.02, 0.95, 5)
+        assert e.value.status == cz.CZ_ERR_INVALID
+    for o in (cz.make_opts(param_bf16=fake + 2), cz.make_opts(debug_update_out=fake + 4),
+              cz.make_opts(grad_is_bf16=True)):
+        pg = fake + 4 if o.grad_is_bf16 else fake        # a bf16 gradient needs 8-byte alignment
+        with pytest.raises(cz.CzError) as e:
+            cz.cz_muon_step_ex(p, 0, fake, pg, fake, args, 0.02, 0.95, 5, None, o)
+        assert e.value.status == cz.CZ_ERR_INVALID
 
 
 def test_workspace_size_grows_with_shard():

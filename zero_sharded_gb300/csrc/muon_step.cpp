@@ -745,6 +745,12 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
   const Plan* p = static_cast<const Plan*>(plan);
   if (rank < 0 || rank >= p->R || ns_steps < 1 || ns_steps > 64) return CZ_ERR_INVALID;
   if (!std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(opts->eps) || opts->eps < 0.f) return CZ_ERR_INVALID;
+  // the kernels move the flat buffers in 16-byte vectors (8 bytes for bf16 ones): their base
+  // addresses must be aligned as any allocation is (a view at an odd element offset is rejected)
+  auto aligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
+  if (!aligned(flat_param, 16) || !aligned(flat_mom, 16) || !aligned(flat_grad, opts->grad_is_bf16 ? 8 : 16) ||
+      !aligned(opts->param_bf16, 8) || !aligned(opts->debug_update_out, 16))
+    return CZ_ERR_INVALID;
   int st = validate_shapes(p, shapes);
   if (st != CZ_OK) return st;
   // parameters must not overlap in the flat layout
