@@ -29,6 +29,8 @@
 #include <utility>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "cz.h"
 
 namespace {
@@ -139,6 +141,7 @@ extern "C" int cz_apply_update(float* flat_param, void* param_bf16, const float*
     if (iv[i].first < iv[i - 1].second) return CZ_ERR_INVALID;   // overlapping tensors would race
   const int st = check_device();
   if (st != CZ_OK) return st;
+  nvtxRangePushA("cz/apply_update");
 
   // 16-byte vectors need the fp32 buffers 16-byte aligned at the tensor's start and the
   // bf16 copy 8-byte aligned there
@@ -167,7 +170,11 @@ extern "C" int cz_apply_update(float* flat_param, void* param_bf16, const float*
     seg.blk_first[seg.n_seg] = (int32_t)blocks;
     apply_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(flat_param, static_cast<__nv_bfloat16*>(param_bf16),
                                                       flat_update, seg);
-    if (cudaGetLastError() != cudaSuccess) return CZ_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) {
+      nvtxRangePop();
+      return CZ_ERR_CUDA;
+    }
   }
+  nvtxRangePop();
   return CZ_OK;
 }

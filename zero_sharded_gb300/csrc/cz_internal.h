@@ -6,11 +6,23 @@
 
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "cz.h"
 
 struct cz_plan {};   // the opaque handle type of the C-ABI; cz::Plan derives from it
 
 namespace cz {
+
+// An NVTX range ("cz/..."), open for the object's lifetime: profilers that record
+// NVTX (Nsight Systems, ncu --nvtx) show the library's host phases by name.  The
+// NVTX3 header is self-contained; with no tool attached a push/pop costs a few ns.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Process-unique id for plans and step programs: caches key on it, never on
 // an address that a later allocation could reuse.

@@ -298,9 +298,15 @@ cudaError_t note(cudaError_t e) {
   return e;
 }
 
-// Launches `fn` on stream s, bracketed by events when tracing is on.
+// NVTX names of the kernel kinds (numbering of cz_profile_read).
+const char* const kKindNames[CZ_KERNEL_KINDS] = {"cz/momentum", "cz/unused",    "cz/ns_gram",  "cz/ns_poly",
+                                                 "cz/ns_update", "cz/ns_update_apply", "cz/ns_fused", "cz/ns_small"};
+
+// Launches `fn` on stream s inside an NVTX range named by its kind, bracketed by
+// events when tracing is on.
 template <class F>
 cudaError_t traced(int kind, cudaStream_t s, F&& fn) {
+  NvtxRange range(kKindNames[kind]);
   if (!g_prof_on) return note(fn());
   ProfRec r{kind, nullptr, nullptr};
   if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return note(cudaGetLastError());
@@ -743,6 +749,7 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
                     const cz_step_opts* opts) {
   if (!plan || !flat_param || !flat_grad || !flat_mom || !offsets || !shapes || !opts) return CZ_ERR_INVALID;
   const Plan* p = static_cast<const Plan*>(plan);
+  NvtxRange range("cz/muon_step");
   if (rank < 0 || rank >= p->R || ns_steps < 1 || ns_steps > 64) return CZ_ERR_INVALID;
   if (!std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(opts->eps) || opts->eps < 0.f) return CZ_ERR_INVALID;
   // the kernels move the flat buffers in 16-byte vectors (8 bytes for bf16 ones): their base

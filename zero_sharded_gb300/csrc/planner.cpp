@@ -149,6 +149,7 @@ int cz_plan_naive(const int64_t* numels, int64_t n_params, const int64_t* bucket
                   int64_t n_buckets, int32_t R, cz_plan** out) {
   if (!out) return CZ_ERR_INVALID;
   *out = nullptr;
+  cz::NvtxRange range("cz/plan_naive");
   int st = check_inputs(numels, n_params, bucket_sizes, n_buckets, R);
   if (st != CZ_OK) return st;
   Plan* p = new_plan(numels, n_params, bucket_sizes, n_buckets, R);
@@ -185,6 +186,7 @@ int cz_plan_partition_cost(const int64_t* numels, const int64_t* costs, int64_t 
                            cz_plan** out) {
   if (!out) return CZ_ERR_INVALID;
   *out = nullptr;
+  cz::NvtxRange range("cz/plan_partition");
   int st = check_inputs(numels, n_params, bucket_sizes, n_buckets, R, costs);
   if (st != CZ_OK) return st;
   if (!(alpha >= 0.0 && alpha <= 1.0)) return CZ_ERR_INVALID;
