@@ -102,7 +102,7 @@ NCU_TRAFFIC = {
                                                     "ns_update": 217.37e6, "ns_update_apply": 618.62e6}}),
     "momentum": ("21a3a013c9d890e1", {"qwen3-1.7b-layer": {"momentum": 649.31e6}}),
     "ns_small": ("021646593652fcc3", {"tiny": {"ns_small": 0.3425e6}}),
-    "apply": ("b875dad85092e1f1", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
+    "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 
 

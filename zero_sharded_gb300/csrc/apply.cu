@@ -155,7 +155,10 @@ extern "C" int cz_apply_update(float* flat_param, void* param_bf16, const float*
     while (i < n_tensors && seg.n_seg < kMaxSeg) {
       const int64_t r = shapes[2 * i], c = shapes[2 * i + 1], n = r * c;
       const int64_t nb = (n + kChunk - 1) / kChunk;
-      if (nb > (int64_t)INT32_MAX) return CZ_ERR_INVALID;
+      if (nb > (int64_t)INT32_MAX) {
+        nvtxRangePop();
+        return CZ_ERR_INVALID;
+      }
       if (blocks + nb > (int64_t)INT32_MAX && seg.n_seg > 0) break;
       const int k = seg.n_seg++;
       seg.off[k] = offsets[i];
