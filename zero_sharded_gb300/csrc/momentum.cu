@@ -21,105 +21,127 @@ namespace cz {
 
 namespace {
 
-constexpr int kTile = 64;
+constexpr int kTileRows = 64;
 constexpr int kThreads = 256;
 constexpr int kTrPitch = 65;   // odd pitch: the transposed smem writes are bank-conflict free
 
-__device__ __forceinline__ void load_grad4(const void* grad, int64_t idx, bool bf16, bool vec, int n_ok,
-                                           float* g) {
+// NQ consecutive gradient values at idx as floats (q >= n_ok: 0).
+template <int NQ>
+__device__ __forceinline__ void load_grad(const void* grad, int64_t idx, bool bf16, bool vec, int n_ok, float* g) {
   if (bf16) {
     const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(grad) + idx;
     if (vec) {
-      uint2 raw = *reinterpret_cast<const uint2*>(gp);
-      __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
-      __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
-      g[0] = __low2float(lo); g[1] = __high2float(lo);
-      g[2] = __low2float(hi); g[3] = __high2float(hi);
+      if constexpr (NQ == 8) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(gp);
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { g[2 * k] = bf16_lo(w[k]); g[2 * k + 1] = bf16_hi(w[k]); }
+      } else {
+        const uint2 raw = *reinterpret_cast<const uint2*>(gp);
+        g[0] = bf16_lo(raw.x); g[1] = bf16_hi(raw.x);
+        g[2] = bf16_lo(raw.y); g[3] = bf16_hi(raw.y);
+      }
     } else {
-      for (int q = 0; q < 4; ++q) g[q] = q < n_ok ? __bfloat162float(gp[q]) : 0.f;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) g[q] = q < n_ok ? __bfloat162float(gp[q]) : 0.f;
     }
   } else {
     const float* gp = static_cast<const float*>(grad) + idx;
     if (vec) {
-      float4 v = __ldcs(reinterpret_cast<const float4*>(gp));
-      g[0] = v.x; g[1] = v.y; g[2] = v.z; g[3] = v.w;
+#pragma unroll
+      for (int k = 0; k < NQ / 4; ++k) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(gp) + k);
+        g[4 * k] = v.x; g[4 * k + 1] = v.y; g[4 * k + 2] = v.z; g[4 * k + 3] = v.w;
+      }
     } else {
-      for (int q = 0; q < 4; ++q) g[q] = q < n_ok ? gp[q] : 0.f;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) g[q] = q < n_ok ? gp[q] : 0.f;
     }
   }
 }
 
-__device__ __forceinline__ uint2 pack_bf16x4(float a, float b, float c, float d) {
-  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(c, d);
-  uint2 r;
-  r.x = *reinterpret_cast<uint32_t*>(&lo);
-  r.y = *reinterpret_cast<uint32_t*>(&hi);
-  return r;
-}
-
+// One block per tile of 64 rows x CW columns of one owned tensor: 16 threads per
+// row, NQ = CW/16 consecutive columns each, four passes of 16 rows.  CW = 64 for
+// fp32 gradients; CW = 128 for bf16 gradients, so that a thread still moves 16-byte
+// gradient vectors (8 bf16) and keeps as many bytes in flight per pass.
+template <int CW>
 __global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
-  __shared__ __nv_bfloat16 trT[kTile * kTrPitch];   // trT[c][r]: the tile, transposed
+  constexpr int NQ = CW / 16;
+  __shared__ __nv_bfloat16 trT[CW * kTrPitch];   // trT[c][r]: the tile, transposed
   __shared__ float warp_sum[kThreads / 32];
 
   const MomTile t = p.tiles[blockIdx.x];
   const MomMat mm = p.mats[t.mat];
   const int tid = threadIdx.x;
-  const bool row_vec = ((mm.off & 3) == 0) && ((mm.cols & 3) == 0);
-  const int cq = (tid & 15) * 4;
+  const bool row_vec = ((mm.off % NQ) == 0) && ((mm.cols % NQ) == 0);
+  const int cq = (tid & 15) * NQ;
   const int rsub = tid >> 4;
   const float mu = p.mu;
   float ss = 0.f;
 
 #pragma unroll
-  for (int pass = 0; pass < 4; ++pass) {
+  for (int pass = 0; pass < kTileRows / 16; ++pass) {
     const int r = rsub + pass * 16;
     const int gr = t.r0 + r;
     const int gc = t.c0 + cq;
-    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    float u[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) u[q] = 0.f;
     if (gr < mm.rows && gc < mm.cols) {
-      const int n_ok = min(4, mm.cols - gc);
+      const int n_ok = min(NQ, mm.cols - gc);
       const int64_t idx = mm.off + (int64_t)gr * mm.cols + gc;
-      const bool vec = row_vec && n_ok == 4;
-      float g[4], m[4];
-      load_grad4(p.grad, idx, p.grad_bf16 != 0, vec, n_ok, g);
+      const bool vec = row_vec && n_ok == NQ;
+      float g[NQ], m[NQ];
+      load_grad<NQ>(p.grad, idx, p.grad_bf16 != 0, vec, n_ok, g);
       float* mp = p.mom + idx;
       if (vec) {
-        float4 v = *reinterpret_cast<const float4*>(mp);
-        m[0] = v.x; m[1] = v.y; m[2] = v.z; m[3] = v.w;
+#pragma unroll
+        for (int k = 0; k < NQ / 4; ++k) {
+          const float4 v = reinterpret_cast<const float4*>(mp)[k];
+          m[4 * k] = v.x; m[4 * k + 1] = v.y; m[4 * k + 2] = v.z; m[4 * k + 3] = v.w;
+        }
       } else {
-        for (int q = 0; q < 4; ++q) m[q] = q < n_ok ? mp[q] : 0.f;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) m[q] = q < n_ok ? mp[q] : 0.f;
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < NQ; ++q) {
         const float mn = __fadd_rn(__fmul_rn(mu, m[q]), g[q]);
         m[q] = mn;
         u[q] = p.nesterov ? __fadd_rn(g[q], __fmul_rn(mu, mn)) : mn;
         if (q >= n_ok) u[q] = 0.f;
       }
       if (vec) {
-        *reinterpret_cast<float4*>(mp) = make_float4(m[0], m[1], m[2], m[3]);
+#pragma unroll
+        for (int k = 0; k < NQ / 4; ++k)
+          reinterpret_cast<float4*>(mp)[k] = make_float4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
       } else {
         for (int q = 0; q < n_ok; ++q) mp[q] = m[q];
       }
       // rows x cols orientation; a partial tail vector lands in the row padding
-      if (mm.direct)
-        *reinterpret_cast<uint2*>(mm.direct + (int64_t)gr * mm.ld_direct + gc) =
-            pack_bf16x4(u[0], u[1], u[2], u[3]);
+      // (the pitch is the column count rounded up to 8)
+      if (mm.direct) {
+        uint16_t* xp = mm.direct + (int64_t)gr * mm.ld_direct + gc;
+        if constexpr (NQ == 8)
+          *reinterpret_cast<uint4*>(xp) = make_uint4(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]),
+                                                     pack_bf16x2(u[4], u[5]), pack_bf16x2(u[6], u[7]));
+        else
+          *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]));
+      }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NQ; ++q) {
       ss = fmaf(u[q], u[q], ss);
       trT[(cq + q) * kTrPitch + r] = __float2bfloat16_rn(u[q]);
     }
   }
   __syncthreads();
-
-  // transposed orientation: rows of u^T are columns of the tile
+  // transposed orientation: rows of u^T are columns of the tile; 16 threads per
+  // u^T row, 4 tile rows (8 bytes) each
 #pragma unroll
-  for (int pass = 0; pass < 4; ++pass) {
+  for (int pass = 0; pass < CW / 16; ++pass) {
     const int c = rsub + pass * 16;
-    const int rq = cq;
+    const int rq = (tid & 15) * 4;
     const int gc = t.c0 + c;
     const int gr = t.r0 + rq;
     if (mm.trans && gc < mm.cols && gr < mm.rows) {
@@ -184,7 +206,8 @@ __global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
 
 cudaError_t launch_momentum(const MomParams& p, cudaStream_t s) {
   if (p.n_tiles <= 0) return cudaSuccess;
-  momentum_kernel<<<p.n_tiles, kThreads, 0, s>>>(p);
+  if (p.grad_bf16) momentum_kernel<kMomTileColsBf16><<<p.n_tiles, kThreads, 0, s>>>(p);
+  else momentum_kernel<kMomTileCols><<<p.n_tiles, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

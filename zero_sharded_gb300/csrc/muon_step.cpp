@@ -456,14 +456,17 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       d.trans = X; d.ld_trans = G.ldx;
     }
     d.tile_first = (int32_t)tcur;
-    const int64_t tr = ceil_div64(om.rows, 64), tc = ceil_div64(om.cols, 64);
+    // momentum tiles: 64 rows x 64 columns, or x 128 with bf16 gradients (the workspace is sized
+    // for 64 x 64, the larger count)
+    const int64_t cw = o.grad_is_bf16 ? kMomTileColsBf16 : kMomTileCols;
+    const int64_t tr = ceil_div64(om.rows, 64), tc = ceil_div64(om.cols, cw);
     d.tile_count = (int32_t)(tr * tc);
     for (int64_t a = 0; a < tr; ++a)
       for (int64_t b = 0; b < tc; ++b) {
         MomTile& t = mt[tcur++];
         t.mat = (int32_t)g;
         t.r0 = (int32_t)(a * 64);
-        t.c0 = (int32_t)(b * 64);
+        t.c0 = (int32_t)(b * cw);
         t.pad = 0;
       }
     MatInfo& m = mi[g];
@@ -481,7 +484,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   mp.mu = mu;
   mp.eps = o.eps;
   mp.tiles = reinterpret_cast<const MomTile*>(ws + L.off_momtiles);
-  mp.n_tiles = (int32_t)L.n_mom_tiles;
+  mp.n_tiles = (int32_t)tcur;   // <= L.n_mom_tiles (64 x 64 tiles), the count the workspace holds
   mp.mats = reinterpret_cast<const MomMat*>(ws + L.off_mommats);
   mp.n_mats = (int32_t)n_mats;
   mp.partial = reinterpret_cast<float*>(ws + L.off_partial);

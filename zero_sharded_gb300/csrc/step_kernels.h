@@ -10,7 +10,12 @@
 namespace cz {
 
 // ------------------------------------------------------------------ momentum pass
-// One 64 x 64 tile of one owned tensor (rows x cols layout of the parameter).
+// Momentum tiles are 64 rows x kMomTileCols columns (fp32 gradients) or 64 x
+// kMomTileColsBf16 (bf16 gradients: 16-byte gradient vectors per thread).
+constexpr int kMomTileCols = 64;
+constexpr int kMomTileColsBf16 = 128;
+
+// One tile of one owned tensor (rows x cols layout of the parameter).
 struct MomTile {
   int32_t mat;     // index into MomMat
   int32_t r0, c0;  // tile origin (element row / column)
