@@ -61,9 +61,10 @@ __device__ __forceinline__ void load_grad(const void* grad, int64_t idx, bool bf
 }
 
 // One block per tile of 64 rows x CW columns of one owned tensor: 16 threads per
-// row, NQ = CW/16 consecutive columns each, four passes of 16 rows.  CW = 64 for
-// fp32 gradients; CW = 128 for bf16 gradients, so that a thread still moves 16-byte
-// gradient vectors (8 bf16) and keeps as many bytes in flight per pass.
+// row, NQ = CW/16 consecutive columns each, four passes of 16 rows.  CW = 128: a
+// thread moves 8 columns per row, so each pass keeps 48 (bf16 gradients) or 64
+// (fp32) bytes in flight per thread (measured: 64 x 64 tiles were 4% slower with
+// fp32 gradients, 11% with bf16).
 template <int CW>
 __global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
   constexpr int NQ = CW / 16;

@@ -456,8 +456,8 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       d.trans = X; d.ld_trans = G.ldx;
     }
     d.tile_first = (int32_t)tcur;
-    // momentum tiles: 64 rows x 64 columns, or x 128 with bf16 gradients (the workspace is sized
-    // for 64 x 64, the larger count)
+    // momentum tiles: 64 rows x kMomTileCols columns (kMomTileColsBf16 with bf16 gradients); the
+    // workspace is sized for 64 x 64 tiles, at least as many
     const int64_t cw = o.grad_is_bf16 ? kMomTileColsBf16 : kMomTileCols;
     const int64_t tr = ceil_div64(om.rows, 64), tc = ceil_div64(om.cols, cw);
     d.tile_count = (int32_t)(tr * tc);

@@ -11,8 +11,9 @@ namespace cz {
 
 // ------------------------------------------------------------------ momentum pass
 // Momentum tiles are 64 rows x kMomTileCols columns (fp32 gradients) or 64 x
-// kMomTileColsBf16 (bf16 gradients: 16-byte gradient vectors per thread).
-constexpr int kMomTileCols = 64;
+// kMomTileColsBf16 (bf16 gradients): 8 columns a thread, so each thread moves two
+// 16-byte vectors of momentum and one (bf16) or two (fp32) of gradient per row.
+constexpr int kMomTileCols = 128;
 constexpr int kMomTileColsBf16 = 128;
 
 // One tile of one owned tensor (rows x cols layout of the parameter).
