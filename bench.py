@@ -98,10 +98,10 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("dccc2a83e4b99620", {"qwen3-1.7b-layer": {"ns_fused": 2640.89e6, "ns_gram": 125.27e6, "ns_poly": 51.42e6,
+    "ns_gemm": ("069a621eb57453b7", {"qwen3-1.7b-layer": {"ns_fused": 2640.89e6, "ns_gram": 125.27e6, "ns_poly": 51.42e6,
                                                     "ns_update": 217.37e6, "ns_update_apply": 618.62e6}}),
-    "momentum": ("21a3a013c9d890e1", {"qwen3-1.7b-layer": {"momentum": 649.31e6}}),
-    "ns_small": ("021646593652fcc3", {"tiny": {"ns_small": 0.3425e6}}),
+    "momentum": ("343ca45a580d9281", {"qwen3-1.7b-layer": {"momentum": 649.81e6}}),
+    "ns_small": ("7694317269f91a57", {"tiny": {"ns_small": 0.3425e6}}),
     "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 
