@@ -408,6 +408,16 @@ def main():
     e2e = None
     if not args.no_e2e:
         Gh = G.to("cpu").pin_memory()
+        # the rank's own tensors only (after a reduce-scatter a ZeRO-1 rank holds just its shard's
+        # gradients): contiguous owned element ranges, one copy each way per range
+        own_rng = []
+        for o_, (r_, c_), ow in sorted(zip(w.offsets, w.shapes, owner)):
+            if ow != my_rank:
+                continue
+            if own_rng and own_rng[-1][1] == o_:
+                own_rng[-1][1] = o_ + r_ * c_
+            else:
+                own_rng.append([o_, o_ + r_ * c_])
         PBh = [torch.empty(PB.shape, dtype=PB.dtype).pin_memory() for _ in range(2)]
         Gd = [G, torch.empty_like(G)]
         PBd = [PB, torch.empty_like(PB)]
@@ -430,7 +440,8 @@ def main():
             with torch.cuda.stream(h2d):
                 if i >= 2:
                     h2d.wait_event(ev_step[i - 2])             # the device buffer's previous user is done
-                Gd[b].copy_(Gh, non_blocking=True)
+                for lo, hi in own_rng:
+                    Gd[b][lo:hi].copy_(Gh[lo:hi], non_blocking=True)
                 ev_h2d[i].record(h2d)
             stream.wait_event(ev_h2d[i])
             if i >= 2:
@@ -439,7 +450,8 @@ def main():
             ev_step[i].record(stream)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(ev_step[i])
-                PBh[b].copy_(PBd[b], non_blocking=True)
+                for lo, hi in own_rng:
+                    PBh[b][lo:hi].copy_(PBd[b][lo:hi], non_blocking=True)
                 ev_d2h[i].record(d2h)
         t1.record(d2h)
         torch.cuda.synchronize()
@@ -448,8 +460,8 @@ def main():
         if world > 1:
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
         e2e = {"value": float(te.item()) / world, "unit": "ms",
-               "h2d_bytes_per_step": int(G.numel() * G.element_size()),
-               "d2h_bytes_per_step": int(PB.numel() * PB.element_size()),
+               "h2d_bytes_per_step": int(sum(hi - lo for lo, hi in own_rng) * G.element_size()),
+               "d2h_bytes_per_step": int(sum(hi - lo for lo, hi in own_rng) * PB.element_size()),
                "overlap": "two copy streams; step j+1's gradient copy and step j's read-back overlap compute",
                "timing": "steady-state pipeline: (end of the last timed read-back - start of the first timed "
                          "gradient copy) / steps, no drain between the warm-up and the timed steps"}

@@ -132,8 +132,10 @@ def test_tiny_config_two_ranks_partition_and_cross_rank_bit_identity():
     [(129, 257), (257, 129), (7, 9), (1, 33), (33, 1)],           # odd sizes: scalar paths, tiny, vectors
     [(512, 512), (384, 1280), (1280, 384), (640, 128)],           # exact tiles, mixed groups
 ])
-def test_ragged_and_multi_tile_shapes(shapes):
-    run = Run(shapes, R=1, seed=3)
+@pytest.mark.parametrize("grad_bf16", [False, True])
+def test_ragged_and_multi_tile_shapes(shapes, grad_bf16):
+    # bf16 gradients: 8-column vectors where offset and width allow, scalar loads elsewhere
+    run = Run(shapes, R=1, seed=3, grad_std=1e-3 if grad_bf16 else 1.0, grad_bf16=grad_bf16)
     run.step()
     check_against_oracle(run, [True] * len(shapes), run.p0, run.m0)
 
