@@ -225,6 +225,35 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle timing
+def torch_library_step(P, G, M, shapes, offsets, lr=LR, mu=MU, steps=NS_STEPS, coeffs=(3.4445, -4.7750, 2.0315),
+                       eps=1e-7):
+    """The same Muon step written with PyTorch library calls, for comparison only (never the product
+    path): fp32 momentum as elementwise ops, the Frobenius norm with torch.linalg, Newton-Schulz in bf16
+    with batched torch.matmul (cuBLAS) per shape group, the apply in fp32."""
+    import torch
+
+    a, b, c = coeffs
+    groups = {}
+    for off, (r, cc) in zip(offsets, shapes):
+        groups.setdefault((min(r, cc), max(r, cc)), []).append((off, r, cc))
+    M.mul_(mu).add_(G)
+    U = G + mu * M
+    for (m, n), items in groups.items():
+        xs = []
+        for off, r, cc in items:
+            u = U[off:off + r * cc].view(r, cc)
+            xs.append(u.t() if r > cc else u)
+        X32 = torch.stack(xs)
+        X = (X32 / (torch.linalg.vector_norm(X32, dim=(1, 2), keepdim=True) + eps)).to(torch.bfloat16)
+        for _ in range(steps):
+            A = X @ X.mT
+            B = b * A + c * (A @ A)
+            X = a * X + B @ X
+        for k, (off, r, cc) in enumerate(items):
+            xk = X[k].float()
+            P[off:off + r * cc].view(r, cc).sub_((xk.t() if r > cc else xk), alpha=lr * max(1.0, r / cc) ** 0.5)
+
+
 def time_oracle_sample(shapes, grad_std, seed=0, max_per_shape=1):
     """Times the fp64 oracle on one tensor of each distinct shape and extrapolates
     to the whole shard by multiplicity.  Returns (ms_per_step, sample_desc, cores)."""
@@ -289,6 +318,7 @@ def main():
                     choices=["qwen3-1.7b-layer", "tiny", "qwen3-1.7b-28L", "qwen3-14b-microgroup", "qwen3-32b-shard"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-torch-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -540,6 +570,25 @@ def main():
                         "peak_source": f"hbm_gbs of {peak_src}"}
     del U
 
+    # the same step through PyTorch library calls (cuBLAS bf16 matmuls per shape group), timed like the
+    # step itself (L2 flushed before each step, CUDA events on the stream): context for what the kernels buy
+    torch_base = None
+    if not args.no_torch_baseline and world == 1:
+        n_tb = max(3, min(args.steps, 5))
+        ev_t = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_tb)]
+        with torch.cuda.stream(stream):
+            torch_library_step(P, G, M, my_shapes, my_offs)
+            for i in range(n_tb):
+                flush.zero_()
+                ev_t[2 * i].record(stream)
+                torch_library_step(P, G, M, my_shapes, my_offs)
+                ev_t[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        tb_ms = statistics.mean(ev_t[2 * i].elapsed_time(ev_t[2 * i + 1]) for i in range(n_tb))
+        torch_base = {"ms_per_step": tb_ms, "steps_timed": n_tb, "speedup_of_this_path": tb_ms / max_ms,
+                      "what": "PyTorch library calls: fp32 momentum elementwise, torch.linalg norm, bf16 batched "
+                              "torch.matmul (cuBLAS) per shape group for Newton-Schulz, fp32 apply; no bf16 copy"}
+
     # planner timing on the 64-layer Qwen3-32B layout (host work, as the pages' "milliseconds" claim)
     full = wl.qwen3_32b_reverse()
     fb = cz.cz_make_buckets(full.numels, full.bucket_cap)
@@ -582,6 +631,7 @@ def main():
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clk, "wall_s_timed_region": wall,
             "planner": planner, "comm_pack": comm_pack, "apply_standalone": apply_standalone,
+            "torch_library_baseline": torch_base,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
