@@ -66,7 +66,7 @@ __device__ __forceinline__ void load_grad(const void* grad, int64_t idx, bool bf
 // (fp32) bytes in flight per thread (measured: 64 x 64 tiles were 4% slower with
 // fp32 gradients, 11% with bf16).
 template <int CW>
-__global__ void __launch_bounds__(kThreads) momentum_kernel(const MomParams p) {
+__global__ void __launch_bounds__(kThreads, 8) momentum_kernel(const MomParams p) {
   constexpr int NQ = CW / 16;
   __shared__ __nv_bfloat16 trT[CW * kTrPitch];   // trT[c][r]: the tile, transposed
   __shared__ float warp_sum[kThreads / 32];
