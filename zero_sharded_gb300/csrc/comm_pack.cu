@@ -48,8 +48,17 @@ __device__ __forceinline__ void copy_bytes(const uint8_t* __restrict__ src, uint
     const int64_t nv = (n - head) >> 4;
     const uint4* sv = reinterpret_cast<const uint4*>(src + head);
     uint4* dv = reinterpret_cast<uint4*>(dst + head);
-    for (int64_t i = tid; i < nv; i += nthr) dv[i] = sv[i];
-    for (int64_t i = head + (nv << 4) + tid; i < n; i += nthr) dst[i] = src[i];
+    // four vectors per thread in flight (loads issued before the stores), then the rest one at a time
+    int64_t i = tid;
+    for (; i + 3 * nthr < nv; i += 4 * nthr) {
+      const uint4 v0 = sv[i], v1 = sv[i + nthr], v2 = sv[i + 2 * nthr], v3 = sv[i + 3 * nthr];
+      dv[i] = v0;
+      dv[i + nthr] = v1;
+      dv[i + 2 * nthr] = v2;
+      dv[i + 3 * nthr] = v3;
+    }
+    for (; i < nv; i += nthr) dv[i] = sv[i];
+    for (int64_t e = head + (nv << 4) + tid; e < n; e += nthr) dst[e] = src[e];
   } else {   // different alignment modulo 16: element-wide copies
     switch (eb) {
       case 8: copy_units<uint64_t>(src, dst, n, tid, nthr); break;
