@@ -176,7 +176,17 @@ def build_workload(name: str, world: int, rank: int):
 
 
 # ------------------------------------------------------------------ clocks
+REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
+    """SM clock and clock-event reasons, read (never set) while the bench runs.
+
+    Preferred: NVML through ctypes, polled every 2 ms in a thread, so that the samples fall inside the
+    timed region (mark_begin / mark_end bracket it; the summary keeps the samples between the marks).
+    Fallback when NVML cannot be loaded: `nvidia-smi -lms 200` for the whole sampler lifetime."""
+
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -184,9 +194,45 @@ class ClockSampler:
     def __init__(self, index: int):
         self.proc = None
         self.index = index
-        self.lines = []
+        self.samples = []              # (time, sm MHz, reason bits)
+        self.t_begin = self.t_end = None
+        self.nvml = None
+        self.thread = None
+        self.stop_flag = False
+        try:
+            import ctypes
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)) != 0:
+                raise OSError("handle")
+            mx = ctypes.c_uint(0)
+            lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx))   # NVML_CLOCK_SM
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nvml = (ctypes, lib, h, reasons)
+            self.max_mhz = float(mx.value)
+        except Exception:
+            self.nvml = None
+
+    def _poll(self):
+        ctypes, lib, h, reasons = self.nvml
+        mhz = ctypes.c_uint(0)
+        bits = ctypes.c_ulonglong(0)
+        while not self.stop_flag:
+            ok = lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(1), ctypes.byref(mhz)) == 0
+            ok = ok and reasons(h, ctypes.byref(bits)) == 0
+            if ok:
+                self.samples.append((time.perf_counter(), float(mhz.value), int(bits.value)))
+            time.sleep(0.002)
 
     def start(self):
+        if self.nvml is not None:
+            import threading
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -194,7 +240,26 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def mark_begin(self):
+        self.t_begin = time.perf_counter()
+
+    def mark_end(self):
+        self.t_end = time.perf_counter()
+
     def stop(self):
+        if self.nvml is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
+            rows = self.samples
+            if self.t_begin is not None and self.t_end is not None:
+                inside = [r for r in rows if self.t_begin <= r[0] <= self.t_end]
+                if inside:
+                    rows = inside
+            if not rows:
+                return None
+            reasons = sorted({nm for _, _, b in rows for bit, nm in REASON_BITS.items() if b & bit})
+            return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(rows), "source": "nvml, 2 ms polls inside the timed region"}
         if self.proc is None:
             return None
         time.sleep(0.25)
@@ -221,7 +286,7 @@ class ClockSampler:
                 if fl.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows), "source": "nvidia-smi -lms 200"}
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -380,6 +445,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
+    clocks.mark_begin()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             flush.zero_()
@@ -387,6 +453,7 @@ def main():
             step()
             ends[i].record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - wall0
