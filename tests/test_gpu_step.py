@@ -342,3 +342,19 @@ def test_low_rank_plus_noise_gradients_track_the_rounding_model():
         assert e_model > UPDATE_TOL          # the case this test is about
         tols.append(1.5 * e_model)
     check_against_oracle(run, [True] * len(shapes), run.p0, run.m0, tol=tols)
+
+
+def test_more_shape_groups_than_one_launch_holds():
+    """40 distinct tiled shapes (a launch's problem table holds 32 groups): every Newton-Schulz product runs as
+    two launches over the groups, the fused launch steps aside, and every tensor still matches the oracle."""
+    shapes = [(130 + i, 260 + 2 * i) if i % 2 == 0 else (260 + 2 * i, 130 + i) for i in range(40)]
+    run = Run(shapes, R=1, seed=17)
+    cz.cz_profile_enable(True)
+    try:
+        run.step()
+        prof = cz.cz_profile_read()
+    finally:
+        cz.cz_profile_enable(False)
+    assert prof["ns_fused"][1] == 0
+    assert prof["ns_gram"][1] == 2 * 5 and prof["ns_poly"][1] == 2 * 5
+    check_against_oracle(run, [True] * len(shapes), run.p0, run.m0)
