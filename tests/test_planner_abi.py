@@ -166,3 +166,17 @@ def test_apply_validation_before_any_gpu_work():
         assert e.value.status == cz.CZ_ERR_INVALID, cse
     st = cz.load().cz_apply_update(fake, None, fake, cz._i64([0]), cz._i64([2, 2]), 1, 0.02, 2, None)
     assert st == cz.CZ_ERR_INVALID                               # shape_scale must be 0 or 1
+
+
+def test_empty_shard_is_a_no_op_without_a_device():
+    """A rank that owns no tensor (more ranks than single-tensor buckets) returns CZ_OK before any
+    device work: the call succeeds here, where there is no GPU to launch on."""
+    numels = [64 * 64, 32 * 128]
+    shapes = [(64, 64), (32, 128)]
+    p = cz.cz_plan_partition(numels, [1, 1], 4, 1.0)
+    owner = p.owner()
+    empty = [r for r in range(4) if r not in owner]
+    assert empty
+    fake = 0x1000
+    for r in empty:
+        cz.cz_muon_step(p, r, fake, fake, fake, cz.StepArgs([0, 4096], shapes), 0.02, 0.95, 5)
