@@ -138,11 +138,12 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   }
   // workspace layout
   const int64_t n_mats = (int64_t)L.mats.size();
-  for (const OwnedMat& om : L.mats) L.n_mom_tiles += ceil_div64(om.rows, 64) * ceil_div64(om.cols, 64);
+  // momentum tiles: 64 rows x kMomTileCols (kMomTileColsBf16 with bf16 gradients); sized for the narrower
+  const int64_t mom_cw = std::min(kMomTileCols, kMomTileColsBf16);
+  for (const OwnedMat& om : L.mats) L.n_mom_tiles += ceil_div64(om.rows, 64) * ceil_div64(om.cols, mom_cw);
   int64_t off = 0;
   L.off_status = off;  off += kAlign;
   L.off_sigma = off;   off = align_up(off + 4 * std::max<int64_t>(n_mats, 1), kAlign);
-  L.off_partial = off; off = align_up(off + 4 * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
   L.off_momtiles = off; off = align_up(off + (int64_t)sizeof(MomTile) * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
   L.off_mommats = off; off = align_up(off + (int64_t)sizeof(MomMat) * std::max<int64_t>(n_mats, 1), kAlign);
   L.off_matinfo = off; off = align_up(off + (int64_t)sizeof(MatInfo) * std::max<int64_t>(n_mats, 1), kAlign);
@@ -175,6 +176,9 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   L.off_cta = off; off = align_up(off + 4 * L.n_cta_entries, kAlign);
   L.off_expect = off; off = align_up(off + 4 * 3 * std::max<int64_t>(n_mats, 1), kAlign);
   L.off_done = off; off = align_up(off + 4 * 3 * kMaxNsSteps * std::max<int64_t>(n_mats, 1), kAlign);
+  // per-tile partial sums of the momentum pass: written before they are read, so outside the tables
+  // that are uploaded on every call
+  L.off_partial = off; off = align_up(off + 4 * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
   for (Group& G : L.groups) {
     G.ldx = align_up(G.n, 8);
     G.ldm = align_up(G.m, 8);
@@ -456,8 +460,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       d.trans = X; d.ld_trans = G.ldx;
     }
     d.tile_first = (int32_t)tcur;
-    // momentum tiles: 64 rows x kMomTileCols columns (kMomTileColsBf16 with bf16 gradients); the
-    // workspace is sized for 64 x 64 tiles, at least as many
+    // momentum tiles: 64 rows x kMomTileCols columns (kMomTileColsBf16 with bf16 gradients)
     const int64_t cw = o.grad_is_bf16 ? kMomTileColsBf16 : kMomTileCols;
     const int64_t tr = ceil_div64(om.rows, 64), tc = ceil_div64(om.cols, cw);
     d.tile_count = (int32_t)(tr * tc);
@@ -484,7 +487,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   mp.mu = mu;
   mp.eps = o.eps;
   mp.tiles = reinterpret_cast<const MomTile*>(ws + L.off_momtiles);
-  mp.n_tiles = (int32_t)tcur;   // <= L.n_mom_tiles (64 x 64 tiles), the count the workspace holds
+  mp.n_tiles = (int32_t)tcur;   // <= L.n_mom_tiles, the count the workspace holds
   mp.mats = reinterpret_cast<const MomMat*>(ws + L.off_mommats);
   mp.n_mats = (int32_t)n_mats;
   mp.partial = reinterpret_cast<float*>(ws + L.off_partial);
