@@ -358,3 +358,17 @@ def test_more_shape_groups_than_one_launch_holds():
     assert prof["ns_fused"][1] == 0
     assert prof["ns_gram"][1] == 2 * 5 and prof["ns_poly"][1] == 2 * 5
     check_against_oracle(run, [True] * len(shapes), run.p0, run.m0)
+
+
+@pytest.mark.parametrize("ns_steps", [2, 6])
+def test_even_step_counts_end_in_the_other_x_buffer(tmp_path, ns_steps):
+    """With an even number of Newton-Schulz steps the last Update (the apply) reads the second X ping-pong
+    buffer: against the oracle, and the fused and per-product launches bit for bit."""
+    shapes = [(384, 1024), (1024, 384), (256, 256)]
+    run = Run(shapes, R=1, seed=21)
+    run.step(ns_steps=ns_steps)
+    check_against_oracle(run, [True] * len(shapes), run.p0, run.m0, ns_steps=ns_steps)
+    on = _run_child(tmp_path, "CZ_NS_FUSED", "1", shapes, ns_steps=ns_steps)
+    off = _run_child(tmp_path, "CZ_NS_FUSED", "0", shapes, ns_steps=ns_steps)
+    assert on["launches"]["ns_fused"] == 2 and off["launches"]["ns_fused"] == 0
+    assert torch.equal(on["P"], off["P"])
