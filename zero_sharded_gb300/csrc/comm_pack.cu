@@ -28,8 +28,8 @@ struct Cuts {
 // alignment modulo 16 (head and tail bytes copied singly), and zero-fill the
 // padding of block r when packing.
 template <typename U>
-__device__ __forceinline__ void copy_units(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t nbytes,
-                                           int64_t tid, int64_t nthr) {
+__device__ __noinline__ void copy_units(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t nbytes,
+                                        int64_t tid, int64_t nthr) {
   const U* s = reinterpret_cast<const U*>(src);
   U* d = reinterpret_cast<U*>(dst);
   const int64_t n = nbytes / (int64_t)sizeof(U);
@@ -50,6 +50,7 @@ __device__ __forceinline__ void copy_bytes(const uint8_t* __restrict__ src, uint
     uint4* dv = reinterpret_cast<uint4*>(dst + head);
     // four vectors per thread in flight (loads issued before the stores), then the rest one at a time
     int64_t i = tid;
+#pragma unroll 1
     for (; i + 3 * nthr < nv; i += 4 * nthr) {
       const uint4 v0 = sv[i], v1 = sv[i + nthr], v2 = sv[i + 2 * nthr], v3 = sv[i + 3 * nthr];
       dv[i] = v0;
@@ -57,6 +58,7 @@ __device__ __forceinline__ void copy_bytes(const uint8_t* __restrict__ src, uint
       dv[i + 2 * nthr] = v2;
       dv[i + 3 * nthr] = v3;
     }
+#pragma unroll 1
     for (; i < nv; i += nthr) dv[i] = sv[i];
     for (int64_t e = head + (nv << 4) + tid; e < n; e += nthr) dst[e] = src[e];
   } else {   // different alignment modulo 16: element-wide copies
