@@ -78,6 +78,20 @@ def test_qwen3_14b_microgroup_full_size():
     _run_full(w, sample)
 
 
+def test_qwen3_1p7b_28_layers_full_size():
+    """28 Qwen3-1.7B layers (196 matrices, 1,409,286,144 elements, byte offsets past
+    5 GB) in one flat buffer: every tensor through the device-side properties, the
+    oracle on the first tensor of each distinct shape and on the buffer's last tensor."""
+    w = wl.qwen3_1p7b_layers(28)
+    assert w.total == 1_409_286_144
+    first = {}
+    for i, s in enumerate(w.shapes):
+        first.setdefault(s, i)
+    sample = sorted(set(first.values()) | {len(w.shapes) - 1})
+    assert len(first) == 4 and w.offsets[-1] * 4 > (5 << 30)
+    _run_full(w, sample)
+
+
 def test_qwen3_32b_heaviest_shard_full_size():
     full = wl.qwen3_32b_reverse()
     b = cz.cz_make_buckets(full.numels, full.bucket_cap)
