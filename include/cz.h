@@ -206,7 +206,13 @@ int cz_workspace_size(const cz_plan* plan, int32_t rank, const int64_t* shapes, 
  * cached workspace for the current device (not safe for concurrent calls on
  * different streams; pass a workspace through cz_muon_step_ex for that).
  * Requires an sm_103a device.  Errors inside kernels (bounded waits that ran out,
- * descriptor checks) are reported by cz_device_status. */
+ * descriptor checks) are reported by cz_device_status.
+ * The first call for a given (plan, rank, buffers, offsets, shapes, workspace,
+ * gradient dtype) builds the step's launch tables on the host and keeps them,
+ * in page-locked host memory, until the library drops its cache of them; later
+ * calls copy them into the workspace with a kernel.  lr, mu, ns_steps and the
+ * scalar options (eps, Nesterov, a, b, c) are launch parameters: changing them
+ * from call to call (a learning-rate schedule) rebuilds nothing. */
 int cz_muon_step(const cz_plan* plan, int32_t rank,
                  float* flat_param, const void* flat_grad, float* flat_mom,
                  const int64_t* offsets, const int64_t* shapes,
@@ -217,6 +223,12 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank,
                     const int64_t* offsets, const int64_t* shapes,
                     float lr, float mu, int32_t ns_steps, void* stream,
                     const cz_step_opts* opts);
+
+/* Number of step programs (launch tables) the library has built since it was
+ * loaded.  Support for checking that a training loop reuses them: it grows only
+ * when a call's plan, rank, buffers, offsets, shapes, workspace or gradient
+ * dtype differ from every cached program's.  No GPU work. */
+int cz_step_programs_built(int64_t* count);
 
 /* cz_muon_step without any device allocation.  The paper has no counterpart
  * to this call; it exists for callers that cannot call cudaMalloc when they run
@@ -235,7 +247,8 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank,
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race.  Device-side errors are recorded in the
  *     array's status word and are not reported by this call.
- * Calls no cudaMalloc, cudaFree or other allocating routine. */
+ * Calls no cudaMalloc, cudaFree or other allocating routine, and page-locks no
+ * host memory: its launch tables are uploaded from pageable memory. */
 #define CZ_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank,
                          float* flat_param, const void* flat_grad, float* flat_mom,
@@ -252,8 +265,8 @@ int cz_device_status(void* stream, void* workspace, int* status_out);
  * launches is bracketed by two CUDA events recorded on the caller's stream;
  * cz_profile_read synchronises on them and returns, per kernel kind, the summed
  * milliseconds and launch counts since the previous read (then clears them).
- * Kinds, in order: 0 momentum pass (including the per-tensor norm), 1 not launched
- * (kept so the numbering stays stable), 2 Gram (A = X X^T),
+ * Kinds, in order: 0 momentum pass (including the per-tensor norm), 1 copy of the
+ * step's launch tables into the workspace, 2 Gram (A = X X^T),
  * 3 Poly (B = bA + cA^2), 4 Update (X <- aX + BX), 5 Update fused with the apply,
  * 6 all Newton-Schulz products of a step in one launch (the default),
  * 7 every Newton-Schulz step of the small matrices (m <= 128, n <= 256) on chip.

@@ -270,6 +270,97 @@ def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
     assert torch.equal(on["P"], plain["P"])
 
 
+_SCHED_CHILD = r"""
+import json, sys, numpy as np, torch
+from zero_sharded_gb300 import cz
+from zero_sharded_gb300 import workloads as wl
+shapes = [tuple(x) for x in json.loads(sys.argv[2])]
+sched = json.loads(sys.argv[3])
+numels = [r * c for r, c in shapes]
+offsets = list(np.cumsum([0] + numels[:-1]))
+args = cz.StepArgs(offsets, shapes)
+plan = cz.cz_plan_partition(numels, [len(shapes)], 1, 1.0)
+p0 = wl.draw(shapes, 0.02, 41)
+g = wl.draw(shapes, 1.0, 42)
+m0 = wl.draw(shapes, 0.5, 43)
+
+
+def bufs():
+    return {"P": p0.cuda(), "G": g.cuda(), "M": m0.cuda(),
+            "PB": torch.zeros(p0.numel(), dtype=torch.bfloat16, device="cuda"),
+            "D": torch.zeros(p0.numel(), device="cuda")}
+
+
+def call(b, sc):
+    o = cz.make_opts(param_bf16=b["PB"], debug_update_out=b["D"], nesterov=sc["nesterov"], eps=sc["eps"],
+                     coeffs=tuple(sc["coeffs"]))
+    cz.cz_muon_step_ex(plan, 0, b["P"], b["G"], b["M"], args, sc["lr"], sc["mu"], 5, None, o)
+    torch.cuda.synchronize()
+    assert cz.cz_device_status(None, None) == cz.CZ_OK
+
+
+n0 = cz.cz_step_programs_built()
+a = bufs()
+call(a, sched[0])                     # builds a's program with the first scalars
+n1 = cz.cz_step_programs_built()
+for k in ("P", "M"):
+    a[k].copy_({"P": p0, "M": m0}[k])
+a["PB"].zero_()
+a["D"].zero_()
+call(a, sched[1])                     # the same program with the second scalars
+n2 = cz.cz_step_programs_built()
+b = bufs()
+call(b, sched[1])                     # other buffers: a program built with the second scalars
+n3 = cz.cz_step_programs_built()
+torch.save({"a": {k: v.cpu() for k, v in a.items()}, "b": {k: v.cpu() for k, v in b.items()},
+            "built": [n1 - n0, n2 - n1, n3 - n2]}, sys.argv[1])
+"""
+
+
+def test_step_scalars_are_launch_parameters(tmp_path):
+    """lr, mu, eps, Nesterov and the Newton-Schulz coefficients can change from call to
+    call (a learning-rate schedule) without a new step program, and a cached program
+    called with new scalars gives, bit for bit, what a program built with them gives;
+    on-chip small, tiled tall and wide, and ragged tensors; fused and per-product
+    launches (one process each), both against the fp64 oracle with the new scalars."""
+    import json
+    import os
+    import subprocess
+    import sys
+    shapes = [(64, 64), (96, 128), (384, 1024), (1024, 384), (300, 520)]
+    sched = [{"lr": 0.02, "mu": 0.95, "eps": 1e-7, "nesterov": True, "coeffs": list(OM.QUINTIC)},
+             {"lr": 0.0031, "mu": 0.8, "eps": 1e-5, "nesterov": False, "coeffs": list(OM.CUBIC)}]
+    out = {}
+    for fused in ("1", "0"):
+        f = tmp_path / f"sched_{fused}.pt"
+        env = dict(os.environ, CZ_NS_FUSED=fused)
+        r = subprocess.run([sys.executable, "-c", _SCHED_CHILD, str(f), json.dumps(shapes), json.dumps(sched)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        out[fused] = torch.load(f)
+    for fused, d in out.items():
+        assert d["built"] == [1, 0, 1], (fused, d["built"])
+        for k in ("P", "M", "PB", "D"):
+            assert torch.equal(d["a"][k], d["b"][k]), (fused, k)
+    for k in ("P", "M", "PB", "D"):
+        assert torch.equal(out["1"]["a"][k], out["0"]["a"][k]), k
+    # the second scalars took effect: the fp64 oracle with them
+    sc = sched[1]
+    numels = [r * c for r, c in shapes]
+    offsets = list(np.cumsum([0] + numels[:-1]))
+    g = wl.draw(shapes, 1.0, 42)
+    m0 = wl.draw(shapes, 0.5, 43)
+    D, M = out["1"]["a"]["D"], out["1"]["a"]["M"]
+    for (r, c), o in zip(shapes, offsets):
+        gi = g[o:o + r * c].reshape(r, c).numpy()
+        mi = m0[o:o + r * c].reshape(r, c).numpy()
+        m_new, _ = OM.momentum(gi, mi, sc["mu"])
+        assert rel_fro(M[o:o + r * c].reshape(r, c).numpy(), m_new) <= MOM_TOL
+        X = OM.orthogonalise(m_new.astype(np.float64), 5, tuple(sc["coeffs"]), eps=sc["eps"])
+        delta = sc["lr"] * OM.shape_scale(r, c) * X
+        assert rel_fro(D[o:o + r * c].reshape(r, c).numpy(), delta) <= UPDATE_TOL, (r, c)
+
+
 SMALL_SHAPES = [(1, 5), (7, 1), (3, 256), (256, 128), (128, 256), (100, 130), (130, 100), (64, 64),
                 (128, 128), (17, 255), (33, 65), (96, 192)]
 

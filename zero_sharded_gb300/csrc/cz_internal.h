@@ -47,4 +47,12 @@ struct Plan : cz_plan {
   double r_lb = 0, j_dp = 0, j_comm = 0;
 };
 
+// The Muon step behind cz_muon_step_ex and cz_muon_step_noalloc.  pin_ok: a new
+// step program may keep its tables in page-locked host memory (copied into the
+// workspace by a kernel on every call); false keeps them in pageable memory
+// (uploaded by cudaMemcpyAsync), for callers that must not page-lock memory.
+int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
+              const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps, void* stream,
+              const cz_step_opts* opts, bool pin_ok);
+
 }  // namespace cz

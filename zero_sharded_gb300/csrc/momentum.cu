@@ -207,6 +207,40 @@ __global__ void __launch_bounds__(kThreads, 8) momentum_kernel(const MomParams p
 
 }  // namespace
 
+// A step program's tables, copied from page-locked host memory: 16-byte loads
+// over the host link with kTablesVec in flight per thread.  The copy is
+// latency-bound (a few hundred KB); with every load issued before the first
+// store it takes about one round trip.
+constexpr int kTablesVec = 4;
+
+__global__ void __launch_bounds__(kThreads) tables_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                               int64_t n) {
+  const int64_t i0 = (int64_t)blockIdx.x * (kThreads * kTablesVec) + threadIdx.x;
+  uint4 v[kTablesVec];
+#pragma unroll
+  for (int q = 0; q < kTablesVec; ++q) {
+    const int64_t i = i0 + (int64_t)q * kThreads;
+    if (i < n) v[q] = src[i];
+  }
+#pragma unroll
+  for (int q = 0; q < kTablesVec; ++q) {
+    const int64_t i = i0 + (int64_t)q * kThreads;
+    if (i < n) dst[i] = v[q];
+  }
+}
+
+cudaError_t launch_tables_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s) {
+  if (bytes <= 0) return cudaSuccess;
+  if ((bytes & 15) || (reinterpret_cast<uintptr_t>(src) & 15) || (reinterpret_cast<uintptr_t>(dst) & 15))
+    return cudaErrorInvalidValue;
+  const int64_t n = bytes >> 4;
+  const int64_t per_block = (int64_t)kThreads * kTablesVec;
+  const int64_t blocks = (n + per_block - 1) / per_block;
+  if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+  tables_copy_kernel<<<(unsigned)blocks, kThreads, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_momentum(const MomParams& p, cudaStream_t s) {
   if (p.n_tiles <= 0) return cudaSuccess;
   if (p.grad_bf16) momentum_kernel<kMomTileColsBf16><<<p.n_tiles, kThreads, 0, s>>>(p);

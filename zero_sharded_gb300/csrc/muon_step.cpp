@@ -260,31 +260,73 @@ struct Launch {
   GemmParams params;
 };
 
-// Everything that depends only on (plan, rank, shapes, offsets, buffers, options).
+// Everything that depends only on (plan, rank, shapes, offsets, buffers, the
+// gradient dtype).  The step's scalars (lr, mu, eps, Nesterov, the Newton-Schulz
+// coefficients) are launch parameters, set on every call.
 struct Program {
   uint64_t uid = next_uid();
   bool pair = true;
   bool fused_ok = false;
   GemmParams fused{};
   Layout L;
-  std::vector<uint8_t> host_tables;   // image of [off_sigma .. off_tiles + tiles) region (tables only)
+  std::vector<uint8_t> host_tables;   // image of the workspace's [tables_begin, tables_end)
   int64_t tables_begin = 0, tables_end = 0;
+  // The same image in page-locked, device-mapped host memory (null when that
+  // allocation failed: the pageable image is uploaded instead), and an event
+  // recorded after every copy out of it, waited on before it is freed.
+  uint8_t* pinned = nullptr;
+  const void* pinned_dev = nullptr;
+  cudaEvent_t copied = nullptr;
   MomParams mom{};
   std::vector<Launch> gram[2], poly, update[2], apply[2];   // [cur]: X buffer read
   SmallParams small{};
+
+  Program() = default;
+  Program(const Program&) = delete;
+  Program& operator=(const Program&) = delete;
+  ~Program() {
+    if (copied) {
+      cudaEventSynchronize(copied);
+      cudaEventDestroy(copied);
+    }
+    if (pinned) cudaFreeHost(pinned);
+  }
 };
+
+// Moves the program's table image into page-locked, device-mapped host memory.
+// On failure the program keeps the pageable image (and the upload by copy).
+void pin_tables(Program& P) {
+  const size_t bytes = P.host_tables.size();
+  if (bytes == 0) return;
+  void* h = nullptr;
+  if (cudaHostAlloc(&h, bytes, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  void* d = nullptr;
+  cudaEvent_t ev = nullptr;
+  if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFreeHost(h);
+    return;
+  }
+  std::memcpy(h, P.host_tables.data(), bytes);
+  P.pinned = static_cast<uint8_t*>(h);
+  P.pinned_dev = d;
+  P.copied = ev;
+  std::vector<uint8_t>().swap(P.host_tables);
+}
 
 struct Key {
   uint64_t plan; int32_t rank; int dev;
   const void *param, *grad, *mom, *pbf16, *dbg, *ws;
-  int32_t grad_bf16, nesterov, ns_steps;
-  float lr, mu, eps, a, b, c;
+  int32_t grad_bf16;
   std::vector<int64_t> offsets, shapes;
   bool operator<(const Key& o) const {
-    return std::tie(plan, rank, dev, param, grad, mom, pbf16, dbg, ws, grad_bf16, nesterov, ns_steps, lr, mu, eps, a,
-                    b, c, offsets, shapes) < std::tie(o.plan, o.rank, o.dev, o.param, o.grad, o.mom, o.pbf16, o.dbg,
-                                                      o.ws, o.grad_bf16, o.nesterov, o.ns_steps, o.lr, o.mu, o.eps,
-                                                      o.a, o.b, o.c, o.offsets, o.shapes);
+    return std::tie(plan, rank, dev, param, grad, mom, pbf16, dbg, ws, grad_bf16, offsets, shapes) <
+           std::tie(o.plan, o.rank, o.dev, o.param, o.grad, o.mom, o.pbf16, o.dbg, o.ws, o.grad_bf16, o.offsets,
+                    o.shapes);
   }
 };
 
@@ -303,7 +345,7 @@ cudaError_t note(cudaError_t e) {
 }
 
 // NVTX names of the kernel kinds (numbering of cz_profile_read).
-const char* const kKindNames[CZ_KERNEL_KINDS] = {"cz/momentum", "cz/unused",    "cz/ns_gram",  "cz/ns_poly",
+const char* const kKindNames[CZ_KERNEL_KINDS] = {"cz/momentum", "cz/tables",    "cz/ns_gram",  "cz/ns_poly",
                                                  "cz/ns_update", "cz/ns_update_apply", "cz/ns_fused", "cz/ns_small"};
 
 // Launches `fn` on stream s inside an NVTX range named by its kind, bracketed by
@@ -324,6 +366,7 @@ cudaError_t traced(int kind, cudaStream_t s, F&& fn) {
 
 std::mutex g_mu;
 std::map<Key, std::shared_ptr<Program>> g_cache;
+int64_t g_programs_built = 0;   // under g_mu
 struct DevWs { void* ptr = nullptr; size_t bytes = 0; };
 std::map<int, DevWs> g_ws;
 
@@ -434,7 +477,8 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   if (st != CZ_OK) return st;
   const int64_t n_mats = (int64_t)L.mats.size();
   P.tables_begin = L.off_sigma;
-  P.tables_end = L.off_expect + 4 * 3 * (int64_t)std::max<size_t>(L.mats.size(), 1);
+  // through the fused launch's completion counters, which the image's zeros reset on every call
+  P.tables_end = align_up(L.off_done + 4 * 3 * kMaxNsSteps * (int64_t)std::max<size_t>(L.mats.size(), 1), 16);
   P.host_tables.assign((size_t)(P.tables_end - P.tables_begin), 0);
   auto& img = P.host_tables;
   const int64_t tb = P.tables_begin;
@@ -476,8 +520,9 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     m.w_off = om.off;
     m.rows = om.rows;
     m.cols = om.cols;
-    m.lrs = (float)((double)lr * std::sqrt(std::max(1.0, (double)om.rows / (double)om.cols)));
+    m.scale = std::sqrt(std::max(1.0, (double)om.rows / (double)om.cols));
     m.vec_ok = ((om.off & 3) == 0 && (om.cols & 3) == 0) ? 1 : 0;
+    m.pad = 0;
   }
   MomParams& mp = P.mom;
   mp.mom = flat_mom;
@@ -503,6 +548,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   common.a = o.a;
   common.b = o.b;
   common.c = o.c;
+  common.lr = lr;
   common.W = flat_param;
   common.Wb = reinterpret_cast<uint16_t*>(o.param_bf16);
   common.dbg = o.debug_update_out;
@@ -617,6 +663,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   sp.a = o.a;
   sp.b = o.b;
   sp.c = o.c;
+  sp.lr = lr;
   sp.W = flat_param;
   sp.Wb = common.Wb;
   sp.dbg = o.debug_update_out;
@@ -750,9 +797,13 @@ int cz_muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const voi
   return cz_muon_step_ex(plan, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, stream, &o);
 }
 
-int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
-                    const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps, void* stream,
-                    const cz_step_opts* opts) {
+}  // extern "C"
+
+namespace cz {
+
+int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
+              const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps, void* stream,
+              const cz_step_opts* opts, bool pin_ok) {
   if (!plan || !flat_param || !flat_grad || !flat_mom || !offsets || !shapes || !opts) return CZ_ERR_INVALID;
   const Plan* p = static_cast<const Plan*>(plan);
   NvtxRange range("cz/muon_step");
@@ -804,8 +855,7 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
   k.plan = p->uid; k.rank = rank; k.dev = dev;
   k.param = flat_param; k.grad = flat_grad; k.mom = flat_mom;
   k.pbf16 = opts->param_bf16; k.dbg = opts->debug_update_out; k.ws = ws;
-  k.grad_bf16 = opts->grad_is_bf16; k.nesterov = opts->nesterov; k.ns_steps = 0;
-  k.lr = lr; k.mu = mu; k.eps = opts->eps; k.a = opts->a; k.b = opts->b; k.c = opts->c;
+  k.grad_bf16 = opts->grad_is_bf16 ? 1 : 0;
   k.offsets.assign(offsets, offsets + p->n_params);
   k.shapes.assign(shapes, shapes + 2 * p->n_params);
   std::shared_ptr<Program> prog;
@@ -817,30 +867,43 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
     st = build_program(p, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, *opts,
                        static_cast<uint8_t*>(ws), *prog);
     if (st != CZ_OK) return st;
+    ++g_programs_built;
+    if (pin_ok) pin_tables(*prog);
     if (g_cache.size() > 64) g_cache.clear();
     g_cache.emplace(k, prog);
   }
-  // The tables (tile lists, per-tensor descriptors) are copied into the
-  // workspace on every call: the caller may have reused the workspace memory
-  // for something else since the last call, even at the same address.
-  if (cudaMemcpyAsync(static_cast<uint8_t*>(ws) + prog->tables_begin, prog->host_tables.data(),
-                      prog->host_tables.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
+  // The tables (tile lists, per-tensor descriptors, zeroed counters) are copied
+  // into the workspace on every call: the caller may have reused the workspace
+  // memory for something else since the last call, even at the same address.
+  const int64_t tbytes = prog->tables_end - prog->tables_begin;
+  uint8_t* tdst = static_cast<uint8_t*>(ws) + prog->tables_begin;
+  if (prog->pinned) {
+    if (traced(1, s, [&] { return launch_tables_copy(prog->pinned_dev, tdst, tbytes, s); }) != cudaSuccess)
+      return CZ_ERR_CUDA;
+    if (cudaEventRecord(prog->copied, s) != cudaSuccess) return CZ_ERR_CUDA;
+  } else if (cudaMemcpyAsync(tdst, prog->host_tables.data(), (size_t)tbytes, cudaMemcpyHostToDevice, s) !=
+             cudaSuccess) {
     return CZ_ERR_CUDA;
+  }
 
   const Program& P = *prog;
-  if (traced(0, s, [&] { return launch_momentum(P.mom, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+  MomParams mp = P.mom;
+  mp.nesterov = opts->nesterov ? 1 : 0;
+  mp.mu = mu;
+  mp.eps = opts->eps;
+  if (traced(0, s, [&] { return launch_momentum(mp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
   if (P.small.n_mats > 0) {
     SmallParams sp = P.small;
     sp.ns_steps = ns_steps;
+    sp.a = opts->a; sp.b = opts->b; sp.c = opts->c; sp.lr = lr;
     if (traced(7, s, [&] { return launch_ns_small(sp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
   }
   GemmParams gp;
+  auto scalars = [&](GemmParams& g) { g.a = opts->a; g.b = opts->b; g.c = opts->c; g.lr = lr; };
   if (P.fused_ok && use_fused() && ns_steps <= kMaxNsSteps) {
-    if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + P.L.off_done, 0,
-                        (size_t)4 * 3 * ns_steps * std::max<size_t>(P.L.mats.size(), 1), s) != cudaSuccess)
-      return CZ_ERR_CUDA;
     gp = P.fused;
     gp.ns_steps = ns_steps;
+    scalars(gp);
     const cudaError_t e = traced(6, s, [&] { return launch_ns_gemm(kFused, P.pair, gp, s); });
     if (e == cudaSuccess) return CZ_OK;
     // The runtime refused the launch (e.g. it cannot guarantee that all units are
@@ -856,21 +919,42 @@ int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const 
     for (const Launch& ln : P.gram[cur]) {
       gp = ln.params;
       gp.first = first;
+      scalars(gp);
       if (traced(2, s, [&] { return launch_ns_gemm(kGram, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
     }
     for (const Launch& ln : P.poly) {
-      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, P.pair, ln.params, s); }) != cudaSuccess)
-        return CZ_ERR_CUDA;
+      gp = ln.params;
+      scalars(gp);
+      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
     }
     const bool final_step = t + 1 == ns_steps;
     const std::vector<Launch>& last = final_step ? P.apply[cur] : P.update[cur];
     for (const Launch& ln : last) {
       gp = ln.params;
       gp.first = first;
+      scalars(gp);
       if (traced(final_step ? 5 : 4, s, [&] { return launch_ns_gemm(ln.phase, P.pair, gp, s); }) != cudaSuccess)
         return CZ_ERR_CUDA;
     }
   }
+  return CZ_OK;
+}
+
+}  // namespace cz
+
+extern "C" {
+
+int cz_muon_step_ex(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
+                    const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps, void* stream,
+                    const cz_step_opts* opts) {
+  return cz::muon_step(plan, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, stream, opts,
+                       true);
+}
+
+int cz_step_programs_built(int64_t* count) {
+  if (!count) return CZ_ERR_INVALID;
+  std::lock_guard<std::mutex> lock(g_mu);
+  *count = g_programs_built;
   return CZ_OK;
 }
 

@@ -53,6 +53,13 @@ struct MomParams {
 
 cudaError_t launch_momentum(const MomParams& p, cudaStream_t s);
 
+// Copies a step program's tables (tile lists, per-tensor descriptors, zeroed
+// counters) from page-locked, device-mapped host memory into the workspace with
+// a kernel: no copy-engine transfer, so the copy neither synchronises the host
+// with the stream (as a pageable upload may) nor queues behind the caller's own
+// host-to-device copies.  src and dst 16-byte aligned, bytes a multiple of 16.
+cudaError_t launch_tables_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s);
+
 // ------------------------------------------------------------------ NS GEMM
 constexpr int kBM = 128;        // UMMA M (TMEM lanes)
 constexpr int kBN = 256;        // UMMA N (TMEM columns per accumulator)
@@ -85,13 +92,23 @@ struct GemmProblem {
   const uint16_t* aux;   int64_t ld_aux, ms_aux;     // kPoly: A (for the b A term)
 };
 
-// Per global matrix: where its parameter lives (for the apply epilogue).
+// Per global matrix: where its parameter lives (for the apply epilogue).  The
+// learning rate is a launch parameter, so the tables hold only the shape scale.
 struct MatInfo {
   int64_t w_off;          // element offset in the flat parameter buffers
+  double scale;           // sqrt(max(1, rows/cols)), in double
   int32_t rows, cols;     // parameter layout
-  float lrs;              // lr * sqrt(max(1, rows/cols))
   int32_t vec_ok;         // w_off and cols are multiples of 4 (16-byte fp32 vectors)
+  int32_t pad;
 };
+
+#ifdef __CUDACC__
+// The apply's coefficient lr * sqrt(max(1, rows/cols)): the product formed in
+// double and rounded to fp32 once, as the host forms it for the standalone apply.
+__device__ __forceinline__ float lr_times_scale(float lr, double scale) {
+  return __double2float_rn(__dmul_rn((double)lr, scale));
+}
+#endif
 
 // One phase's tile list inside a fused launch.
 struct TileList {
@@ -116,6 +133,7 @@ struct GemmParams {
   const float* sigma;     // per global matrix
   const MatInfo* mats;    // per global matrix
   float a, b, c;
+  float lr;               // learning rate (kApply)
   int32_t first;          // 1: Newton-Schulz step 1 (scale by sigma)
   float* W;               // fp32 master (kApply)
   uint16_t* Wb;           // bf16 copy or null (kApply)
@@ -173,6 +191,7 @@ struct SmallParams {
   const float* sigma;     // per global matrix
   const MatInfo* info;    // per global matrix
   float a, b, c;
+  float lr;               // learning rate
   float* W;               // fp32 master
   uint16_t* Wb;           // bf16 copy or null
   float* dbg;             // debug delta or null

@@ -76,5 +76,7 @@ extern "C" int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank, float* fl
   if (st != CZ_OK) return st;
   o.workspace = scratch;
   o.workspace_bytes = (size_t)CZ_STATIC_WORKSPACE_BYTES;
-  return cz_muon_step_ex(plan, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, stream, &o);
+  // tables stay in pageable memory: page-locking host memory can synchronise like cudaMalloc
+  return cz::muon_step(plan, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, stream, &o,
+                       false);
 }

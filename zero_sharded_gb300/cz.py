@@ -95,6 +95,7 @@ def load() -> ctypes.CDLL:
                                                 ctypes.c_void_p, _i64p, _i64p, ctypes.c_float, ctypes.c_float,
                                                 ctypes.c_int32, ctypes.c_void_p, ctypes.POINTER(cz_step_opts)]),
         "cz_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, _i32p]),
+        "cz_step_programs_built": (ctypes.c_int, [_i64p]),
         "cz_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
         "cz_profile_read": (ctypes.c_int, [_f64p, _i64p, ctypes.c_int32]),
         "cz_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
@@ -335,7 +336,13 @@ def cz_device_status(stream=None, workspace=None) -> int:
     return v.value
 
 
-KERNEL_KINDS = ("momentum", "norm_finalize", "ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused",
+def cz_step_programs_built() -> int:
+    v = ctypes.c_int64(0)
+    _check("cz_step_programs_built", load().cz_step_programs_built(ctypes.byref(v)))
+    return v.value
+
+
+KERNEL_KINDS = ("momentum", "tables", "ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused",
                 "ns_small")
 
 
