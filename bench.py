@@ -98,10 +98,9 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("87b8f07518b8ba6e", {"qwen3-1.7b-layer": {"ns_fused": 2640.89e6, "ns_gram": 125.27e6, "ns_poly": 51.42e6,
-                                                    "ns_update": 217.37e6, "ns_update_apply": 618.62e6}}),
-    "momentum": ("8d2d7e25a87e8a1b", {"qwen3-1.7b-layer": {"momentum": 649.90e6}}),
-    "ns_small": ("454c84d36e6f72dd", {"tiny": {"ns_small": 0.3425e6}}),
+    "ns_gemm": ("17df34875acfd658", {"qwen3-1.7b-layer": {"ns_fused": 2619.04e6}}),
+    "momentum": ("ed0601f9fd8c918f", {"qwen3-1.7b-layer": {"momentum": 646.24e6}}),
+    "ns_small": ("76af3f924d6b117f", {"tiny": {"ns_small": 0.3428e6}}),
     "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 
