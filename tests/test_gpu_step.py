@@ -361,6 +361,52 @@ def test_step_scalars_are_launch_parameters(tmp_path):
         assert rel_fro(D[o:o + r * c].reshape(r, c).numpy(), delta) <= UPDATE_TOL, (r, c)
 
 
+_EVICT_CHILD = r"""
+import sys, numpy as np, torch
+from zero_sharded_gb300 import cz
+from zero_sharded_gb300 import workloads as wl
+w = wl.tiny()
+plan = cz.cz_plan_partition(w.numels, [len(w.shapes)], 1, 1.0)
+args = cz.StepArgs(w.offsets, w.shapes)
+p0 = wl.draw(w.shapes, 0.02, 5).cuda()
+G = wl.draw(w.shapes, 1.0, 6).cuda()
+P, M = p0.clone(), torch.zeros_like(p0)
+n = int(sys.argv[2])
+D = [torch.zeros_like(p0) for _ in range(n)]
+n0 = cz.cz_step_programs_built()
+for k in list(range(n)) + [0]:          # n distinct programs, then the first (evicted) again
+    P.copy_(p0)
+    M.zero_()
+    cz.cz_muon_step_ex(plan, 0, P, G, M, args, 0.02, 0.95, 5, None, cz.make_opts(debug_update_out=D[k]))
+torch.cuda.synchronize()
+assert cz.cz_device_status(None, None) == cz.CZ_OK
+built = cz.cz_step_programs_built() - n0
+same = all(torch.equal(D[0], d) for d in D)
+torch.save({"built": built, "same": same, "D0": D[0].cpu(), "P": P.cpu()}, sys.argv[1])
+"""
+
+
+def test_program_cache_eviction_frees_page_locked_tables(tmp_path):
+    """More distinct step programs than the cache keeps (64): the cache is cleared,
+    each evicted program waits for its last table copy before its page-locked image
+    is freed, an evicted program is rebuilt when its key returns, every call gives
+    the same delta bit for bit, and the process exits cleanly with programs alive."""
+    import subprocess
+    import sys
+    n = 70
+    f = tmp_path / "evict.pt"
+    r = subprocess.run([sys.executable, "-c", _EVICT_CHILD, str(f), str(n)], capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = torch.load(f)
+    assert d["built"] == n + 1
+    assert d["same"]
+    w = wl.tiny()
+    p0 = wl.draw(w.shapes, 0.02, 5)
+    assert torch.equal(d["P"], p0 - d["D0"])      # the last call (a rebuilt program) applied that delta
+    assert float(d["D0"].abs().max()) > 0
+
+
 SMALL_SHAPES = [(1, 5), (7, 1), (3, 256), (256, 128), (128, 256), (100, 130), (130, 100), (64, 64),
                 (128, 128), (17, 255), (33, 65), (96, 192)]
 
