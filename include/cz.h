@@ -212,7 +212,15 @@ int cz_workspace_size(const cz_plan* plan, int32_t rank, const int64_t* shapes, 
  * in page-locked host memory, until the library drops its cache of them; later
  * calls copy them into the workspace with a kernel.  lr, mu, ns_steps and the
  * scalar options (eps, Nesterov, a, b, c) are launch parameters: changing them
- * from call to call (a learning-rate schedule) rebuilds nothing. */
+ * from call to call (a learning-rate schedule) rebuilds nothing.
+ * CUDA graphs: a call may be enqueued into a stream that is being captured,
+ * once a call with the same (plan, rank, buffers, offsets, shapes, workspace,
+ * gradient dtype) has run outside the capture and the workspace (the caller's,
+ * or the library's cached one, already large enough) exists; otherwise the call
+ * returns CZ_ERR_INVALID before enqueuing anything.  The graph replays the
+ * captured scalars (lr, mu, ...) and reads the buffers in place; the library
+ * keeps the captured program's page-locked tables until the process exits.
+ * Kernel timing (cz_profile_enable) skips captured launches. */
 int cz_muon_step(const cz_plan* plan, int32_t rank,
                  float* flat_param, const void* flat_grad, float* flat_mom,
                  const int64_t* offsets, const int64_t* shapes,
@@ -242,13 +250,13 @@ int cz_step_programs_built(int64_t* count);
  *   - A shard whose cz_workspace_size exceeds CZ_STATIC_WORKSPACE_BYTES is
  *     rejected with CZ_ERR_NOMEM before any GPU work.
  *   - The first call on each device does a set-up (looks up the array's device
- *     address and clears its status word, synchronously); make that first call
- *     before any stream capture.
+ *     address and clears its status word, synchronously).
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race.  Device-side errors are recorded in the
  *     array's status word and are not reported by this call.
  * Calls no cudaMalloc, cudaFree or other allocating routine, and page-locks no
- * host memory: its launch tables are uploaded from pageable memory. */
+ * host memory: its launch tables are uploaded from pageable memory, so it cannot
+ * be captured into a CUDA graph (CZ_ERR_INVALID inside a capture). */
 #define CZ_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank,
                          float* flat_param, const void* flat_grad, float* flat_mom,

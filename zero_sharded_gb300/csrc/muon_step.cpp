@@ -277,6 +277,9 @@ struct Program {
   uint8_t* pinned = nullptr;
   const void* pinned_dev = nullptr;
   cudaEvent_t copied = nullptr;
+  // Used inside a stream capture: a CUDA graph may replay the copy out of the
+  // page-locked image at any later time, so the image is never freed.
+  bool captured = false;
   MomParams mom{};
   std::vector<Launch> gram[2], poly, update[2], apply[2];   // [cur]: X buffer read
   SmallParams small{};
@@ -289,7 +292,7 @@ struct Program {
       cudaEventSynchronize(copied);
       cudaEventDestroy(copied);
     }
-    if (pinned) cudaFreeHost(pinned);
+    if (pinned && !captured) cudaFreeHost(pinned);
   }
 };
 
@@ -350,10 +353,14 @@ const char* const kKindNames[CZ_KERNEL_KINDS] = {"cz/momentum", "cz/tables",    
 
 // Launches `fn` on stream s inside an NVTX range named by its kind, bracketed by
 // events when tracing is on.
+// Set while a call enqueues into a stream that is being captured: no timing
+// events are recorded then (a captured event record is not a timing point).
+thread_local bool t_capturing = false;
+
 template <class F>
 cudaError_t traced(int kind, cudaStream_t s, F&& fn) {
   NvtxRange range(kKindNames[kind]);
-  if (!g_prof_on) return note(fn());
+  if (!g_prof_on || t_capturing) return note(fn());
   ProfRec r{kind, nullptr, nullptr};
   if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return note(cudaGetLastError());
   cudaEventRecord(r.a, s);
@@ -736,11 +743,12 @@ int check_device() {
   return CZ_OK;
 }
 
-int get_internal_ws(size_t need, void** out) {
+int get_internal_ws(size_t need, void** out, bool capturing) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CZ_ERR_CUDA;
   DevWs& w = g_ws[dev];
   if (w.bytes < need) {
+    if (capturing) return CZ_ERR_INVALID;   // growing it synchronises and allocates
     if (w.ptr) {
       cudaDeviceSynchronize();
       cudaFree(w.ptr);
@@ -839,17 +847,26 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   if (st != CZ_OK) return st;
 
   std::lock_guard<std::mutex> lock(g_mu);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Inside a stream capture the call may only enqueue: no table build, no
+  // allocation, no pageable upload (none of them can be captured).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (note(cudaStreamIsCapturing(s, &cap)) != cudaSuccess) return CZ_ERR_CUDA;
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+  struct CaptureFlag {
+    explicit CaptureFlag(bool on) { t_capturing = on; }
+    ~CaptureFlag() { t_capturing = false; }
+  } capture_flag(capturing);
   void* ws = opts->workspace;
   if (ws) {
     if (opts->workspace_bytes < need) return CZ_ERR_NOMEM;
     if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0) return CZ_ERR_INVALID;
   } else {
-    st = get_internal_ws(need, &ws);
+    st = get_internal_ws(need, &ws, capturing);
     if (st != CZ_OK) return st;
   }
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   Key k;
   k.plan = p->uid; k.rank = rank; k.dev = dev;
@@ -863,6 +880,7 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   if (it != g_cache.end()) {
     prog = it->second;
   } else {
+    if (capturing) return CZ_ERR_INVALID;   // the first call for these buffers must run outside the capture
     prog = std::make_shared<Program>();
     st = build_program(p, rank, flat_param, flat_grad, flat_mom, offsets, shapes, lr, mu, ns_steps, *opts,
                        static_cast<uint8_t*>(ws), *prog);
@@ -877,10 +895,12 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   // memory for something else since the last call, even at the same address.
   const int64_t tbytes = prog->tables_end - prog->tables_begin;
   uint8_t* tdst = static_cast<uint8_t*>(ws) + prog->tables_begin;
+  if (capturing && !prog->pinned) return CZ_ERR_INVALID;   // a pageable upload cannot be captured
   if (prog->pinned) {
     if (traced(1, s, [&] { return launch_tables_copy(prog->pinned_dev, tdst, tbytes, s); }) != cudaSuccess)
       return CZ_ERR_CUDA;
-    if (cudaEventRecord(prog->copied, s) != cudaSuccess) return CZ_ERR_CUDA;
+    if (capturing) prog->captured = true;
+    else if (cudaEventRecord(prog->copied, s) != cudaSuccess) return CZ_ERR_CUDA;
   } else if (cudaMemcpyAsync(tdst, prog->host_tables.data(), (size_t)tbytes, cudaMemcpyHostToDevice, s) !=
              cudaSuccess) {
     return CZ_ERR_CUDA;

@@ -67,6 +67,14 @@ extern "C" int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank, float* fl
   } else {
     cz_step_opts_default(&o);
   }
+  // a pageable upload cannot be captured, and the first call's set-up synchronises:
+  // refuse a capturing stream before anything else
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return CZ_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return CZ_ERR_INVALID;
   size_t need = 0;
   int st = cz_workspace_size(plan, rank, shapes, &need);
   if (st != CZ_OK) return st;
