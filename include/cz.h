@@ -180,6 +180,10 @@ typedef struct {
   size_t  workspace_bytes;
   float*  debug_update_out;/* nullable: fp32 flat buffer (param layout); receives
                               lr*sqrt(max(1,rows/cols))*X_K for owned tensors          */
+  const float* lr_device;  /* nullable: a device float (4-byte aligned) that the apply
+                              reads in place of the lr argument, when the launch runs;
+                              a step captured in a CUDA graph then follows a schedule
+                              written there before each replay                         */
 } cz_step_opts;
 
 void cz_step_opts_default(cz_step_opts* opts);

@@ -76,6 +76,36 @@ for k in range(3):
 assert cz.cz_device_status(None, g["WS"]) == cz.CZ_OK
 rebuilt = cz.cz_step_programs_built() - built
 
+# a schedule through lr_device: eager calls with lr = 0.02, 0.01, 0.005 against replays of one capture
+# that reads lr from device memory written before each replay
+sched = [0.02, 0.01, 0.005]
+e2 = state()
+eager2 = []
+for k, lr in enumerate(sched):
+    e2["G"].copy_(grads[k])
+    o = cz.make_opts(param_bf16=e2["PB"], workspace=e2["WS"], workspace_bytes=ws_bytes)
+    cz.cz_muon_step_ex(plan, 0, e2["P"], e2["G"], e2["M"], args, lr, MU, 5, s0, o)
+    torch.cuda.synchronize()
+    eager2.append((e2["P"].clone(), e2["M"].clone(), e2["PB"].clone()))
+lr_t = torch.full((1,), 123.0, device="cuda")     # the lr argument below is never used
+h = state()
+oh = cz.make_opts(param_bf16=h["PB"], workspace=h["WS"], workspace_bytes=ws_bytes, lr_device=lr_t)
+cz.cz_muon_step_ex(plan, 0, h["P"], h["G"], h["M"], args, 9.0, MU, 5, s0, oh)
+torch.cuda.synchronize()
+h["P"].copy_(p0)
+h["M"].zero_()
+h["PB"].zero_()
+graph3 = torch.cuda.CUDAGraph()
+with torch.cuda.graph(graph3, stream=cap):
+    cz.cz_muon_step_ex(plan, 0, h["P"], h["G"], h["M"], args, 9.0, MU, 5, torch.cuda.current_stream(), oh)
+same_sched = []
+for k, lr in enumerate(sched):
+    h["G"].copy_(grads[k])
+    lr_t.fill_(lr)
+    graph3.replay()
+    torch.cuda.synchronize()
+    same_sched.append([torch.equal(a, b) for a, b in zip((h["P"], h["M"], h["PB"]), eager2[k])])
+
 # refused inside a capture: buffers without an eager call first, and the allocation-free entry point
 f = state()
 refused = []
@@ -93,7 +123,7 @@ with torch.cuda.graph(graph2, stream=cap):
         refused.append(err.status)
     f["P"].add_(0.0)      # keeps the captured graph non-empty
 torch.cuda.synchronize()
-json.dump({"same": same, "rebuilt": rebuilt, "refused": refused,
+json.dump({"same": same, "same_sched": same_sched, "rebuilt": rebuilt, "refused": refused,
            "invalid": cz.CZ_ERR_INVALID}, open(sys.argv[1], "w"))
 """
 
@@ -102,8 +132,10 @@ json.dump({"same": same, "rebuilt": rebuilt, "refused": refused,
 def test_step_replayed_from_a_cuda_graph(tmp_path, fused):
     """Three replays of a captured step (new gradients copied in before each) equal three
     eager steps bit for bit (fp32 master, momentum, bf16 copy), with the fused launch and
-    with one launch per product; capturing builds nothing; a first call for new buffers
-    and the allocation-free entry point are refused inside a capture."""
+    with one launch per product; a capture that reads lr from device memory follows a
+    schedule written there before each replay, bit for bit as eager calls with those lr;
+    capturing builds nothing; a first call for new buffers and the allocation-free entry
+    point are refused inside a capture."""
     shapes = [(64, 64), (96, 128), (384, 1024), (1024, 384), (300, 520)]
     f = tmp_path / f"graph_{fused}.json"
     env = dict(os.environ, CZ_NS_FUSED=fused)
@@ -112,5 +144,6 @@ def test_step_replayed_from_a_cuda_graph(tmp_path, fused):
     assert r.returncode == 0, r.stderr[-3000:]
     d = json.loads(f.read_text())
     assert d["same"] == [[True, True, True]] * 3, d["same"]
+    assert d["same_sched"] == [[True, True, True]] * 3, d["same_sched"]
     assert d["rebuilt"] == 0
     assert d["refused"] == [d["invalid"], d["invalid"]], d["refused"]

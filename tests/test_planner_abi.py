@@ -129,7 +129,7 @@ def test_step_validation_before_any_gpu_work():
             cz.cz_muon_step(p, 0, *bad, args, 0.02, 0.95, 5)
         assert e.value.status == cz.CZ_ERR_INVALID
     for o in (cz.make_opts(param_bf16=fake + 2), cz.make_opts(debug_update_out=fake + 4),
-              cz.make_opts(grad_is_bf16=True)):
+              cz.make_opts(grad_is_bf16=True), cz.make_opts(lr_device=fake + 2)):
         pg = fake + 4 if o.grad_is_bf16 else fake        # a bf16 gradient needs 8-byte alignment
         with pytest.raises(cz.CzError) as e:
             cz.cz_muon_step_ex(p, 0, fake, pg, fake, args, 0.02, 0.95, 5, None, o)

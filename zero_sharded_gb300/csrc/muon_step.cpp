@@ -821,7 +821,7 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   // addresses must be aligned as any allocation is (a view at an odd element offset is rejected)
   auto aligned = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
   if (!aligned(flat_param, 16) || !aligned(flat_mom, 16) || !aligned(flat_grad, opts->grad_is_bf16 ? 8 : 16) ||
-      !aligned(opts->param_bf16, 8) || !aligned(opts->debug_update_out, 16))
+      !aligned(opts->param_bf16, 8) || !aligned(opts->debug_update_out, 16) || !aligned(opts->lr_device, 4))
     return CZ_ERR_INVALID;
   int st = validate_shapes(p, shapes);
   if (st != CZ_OK) return st;
@@ -915,11 +915,13 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   if (P.small.n_mats > 0) {
     SmallParams sp = P.small;
     sp.ns_steps = ns_steps;
-    sp.a = opts->a; sp.b = opts->b; sp.c = opts->c; sp.lr = lr;
+    sp.a = opts->a; sp.b = opts->b; sp.c = opts->c; sp.lr = lr; sp.lr_dev = opts->lr_device;
     if (traced(7, s, [&] { return launch_ns_small(sp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
   }
   GemmParams gp;
-  auto scalars = [&](GemmParams& g) { g.a = opts->a; g.b = opts->b; g.c = opts->c; g.lr = lr; };
+  auto scalars = [&](GemmParams& g) {
+    g.a = opts->a; g.b = opts->b; g.c = opts->c; g.lr = lr; g.lr_dev = opts->lr_device;
+  };
   if (P.fused_ok && use_fused() && ns_steps <= kMaxNsSteps) {
     gp = P.fused;
     gp.ns_steps = ns_steps;

@@ -195,7 +195,7 @@ constexpr int kApplyPitch = 20;   // floats per staged row (16 + 4): conflict-fr
 
 __device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProblem& pr, const MatInfo& mi, int rbase,
                                             int col0, const float* v, Pre& pre, float* stage, int lane) {
-  const float lrs = lr_times_scale(p.lr, mi.scale);
+  const float lrs = lr_times_scale(p.lr_dev ? __ldg(p.lr_dev) : p.lr, mi.scale);
   if (mi.rows > mi.cols && mi.vec_ok) {
     // tall W = X^T with 16-byte W access: the chunk's delta goes through smem transposed (W row jj =
     // D column, 32 floats per row; 4-float groups XOR-swizzled by the row's parity, so both the

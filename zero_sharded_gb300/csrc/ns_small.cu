@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) ns_small_kernel(const SmallPara
       // conflict-free both along rows and down columns), then W updated along its rows
       float* S = reinterpret_cast<float*>(base);
       const int pitch = n_pad + 1;
-      const float lrs = lr_times_scale(p.lr, mi.scale);
+      const float lrs = lr_times_scale(p.lr_dev ? __ldg(p.lr_dev) : p.lr, mi.scale);
 #pragma unroll 1
       for (int j = 0; j < (n_pad >> 5); ++j) {
         float v[32];

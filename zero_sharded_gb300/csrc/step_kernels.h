@@ -134,6 +134,7 @@ struct GemmParams {
   const MatInfo* mats;    // per global matrix
   float a, b, c;
   float lr;               // learning rate (kApply)
+  const float* lr_dev;    // or null: the learning rate in device memory, read in place of lr
   int32_t first;          // 1: Newton-Schulz step 1 (scale by sigma)
   float* W;               // fp32 master (kApply)
   uint16_t* Wb;           // bf16 copy or null (kApply)
@@ -192,6 +193,7 @@ struct SmallParams {
   const MatInfo* info;    // per global matrix
   float a, b, c;
   float lr;               // learning rate
+  const float* lr_dev;    // or null: the learning rate in device memory, read in place of lr
   float* W;               // fp32 master
   uint16_t* Wb;           // bf16 copy or null
   float* dbg;             // debug delta or null

@@ -40,6 +40,7 @@ class cz_step_opts(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("debug_update_out", ctypes.c_void_p),
+        ("lr_device", ctypes.c_void_p),
     ]
 
 
@@ -315,8 +316,9 @@ def cz_muon_step_noalloc(plan: Plan, rank: int, flat_param, flat_grad, flat_mom,
 
 def make_opts(param_bf16=None, workspace=None, workspace_bytes: int = 0, debug_update_out=None,
               grad_is_bf16: bool = False, nesterov: bool = True, eps: Optional[float] = None,
-              coeffs: Optional[Tuple[float, float, float]] = None) -> cz_step_opts:
+              coeffs: Optional[Tuple[float, float, float]] = None, lr_device=None) -> cz_step_opts:
     o = cz_step_opts_default()
+    o.lr_device = _ptr(lr_device)
     o.param_bf16 = _ptr(param_bf16)
     o.workspace = _ptr(workspace)
     o.workspace_bytes = int(workspace_bytes)
