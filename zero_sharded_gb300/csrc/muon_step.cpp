@@ -280,6 +280,11 @@ struct Program {
   // Used inside a stream capture: a CUDA graph may replay the copy out of the
   // page-locked image at any later time, so the image is never freed.
   bool captured = false;
+  // The small-matrix launch runs on a side stream, beside the tiled products,
+  // when both fit on the GPU at once (forked after the momentum pass, joined
+  // before the call's work ends); events of this program.
+  bool fork_small = false;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   MomParams mom{};
   std::vector<Launch> gram[2], poly, update[2], apply[2];   // [cur]: X buffer read
   SmallParams small{};
@@ -293,6 +298,8 @@ struct Program {
       cudaEventDestroy(copied);
     }
     if (pinned && !captured) cudaFreeHost(pinned);
+    if (fork_ev) cudaEventDestroy(fork_ev);
+    if (join_ev) cudaEventDestroy(join_ev);
   }
 };
 
@@ -648,9 +655,18 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       app[cur].push_back(e);
     }
   }
+  // Units of every GEMM launch: no more than the most tiles of any one product
+  // list, so that a shard of a few small tiles leaves the rest of the GPU free.
+  int64_t most = 1;
+  for (auto* v : {&gram[0], &poly, &upd[0], &app[0]}) {
+    int64_t t = 0;
+    for (const ProbDesc& d : *v) t += (int64_t)d.tiles.size();
+    most = std::max(most, t);
+  }
+  const int units = (int)std::min<int64_t>(max_grid, most);
   // Gram with first=0/1 share one tile list: build first, copy for the other flag.
   auto ml = [&](int phase, std::vector<ProbDesc>& probs, std::vector<Launch>& out, int cur) {
-    make_launches(phase, probs, dev_tiles, host_tiles, cursor, dev_cta, host_cta, cta_cursor, max_grid, common, out,
+    make_launches(phase, probs, dev_tiles, host_tiles, cursor, dev_cta, host_cta, cta_cursor, units, common, out,
                   0, cur);
   };
   ml(kGram, gram[0], P.gram[0], 0);
@@ -730,7 +746,37 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     F.done = reinterpret_cast<int*>(ws + L.off_done);
     P.fused_ok = true;
   }
+  // The small-matrix CTAs beside the tiled products' units: only when all of them
+  // fit on the GPU at once (then neither waits for the other's SMs).
+  bool tiled = false;
+  for (const Group& G : L.groups) tiled |= !G.small;
+  int dev = 0, sms = 0;
+  if (n_small > 0 && tiled && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      (int64_t)units * (pair ? 2 : 1) + n_small <= sms) {
+    if (cudaEventCreateWithFlags(&P.fork_ev, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&P.join_ev, cudaEventDisableTiming) == cudaSuccess)
+      P.fork_small = true;
+    else
+      cudaGetLastError();
+  }
   return CZ_OK;
+}
+
+// The library's side stream of the current device (non-blocking, never destroyed).
+cudaStream_t side_stream() {
+  static std::map<int, cudaStream_t> streams;   // callers hold g_mu
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  auto it = streams.find(dev);
+  if (it != streams.end()) return it->second;
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  streams.emplace(dev, st);
+  return st;
 }
 
 int check_device() {
@@ -912,11 +958,30 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   mp.mu = mu;
   mp.eps = opts->eps;
   if (traced(0, s, [&] { return launch_momentum(mp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+  // joins the side stream back into s on every return path once it has been forked
+  struct Join {
+    cudaStream_t s = nullptr;
+    cudaEvent_t ev = nullptr;
+    ~Join() {
+      if (ev) cudaStreamWaitEvent(s, ev, 0);
+    }
+  } join;
   if (P.small.n_mats > 0) {
     SmallParams sp = P.small;
     sp.ns_steps = ns_steps;
     sp.a = opts->a; sp.b = opts->b; sp.c = opts->c; sp.lr = lr; sp.lr_dev = opts->lr_device;
-    if (traced(7, s, [&] { return launch_ns_small(sp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
+    cudaStream_t side = (P.fork_small && !capturing) ? side_stream() : nullptr;
+    if (side) {
+      if (cudaEventRecord(P.fork_ev, s) != cudaSuccess || cudaStreamWaitEvent(side, P.fork_ev, 0) != cudaSuccess)
+        return CZ_ERR_CUDA;
+      const cudaError_t e = traced(7, side, [&] { return launch_ns_small(sp, side); });
+      if (cudaEventRecord(P.join_ev, side) != cudaSuccess) return CZ_ERR_CUDA;
+      join.s = s;
+      join.ev = P.join_ev;
+      if (e != cudaSuccess) return CZ_ERR_CUDA;
+    } else if (traced(7, s, [&] { return launch_ns_small(sp, s); }) != cudaSuccess) {
+      return CZ_ERR_CUDA;
+    }
   }
   GemmParams gp;
   auto scalars = [&](GemmParams& g) {
