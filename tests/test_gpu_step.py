@@ -407,6 +407,37 @@ def test_program_cache_eviction_frees_page_locked_tables(tmp_path):
     assert float(d["D0"].abs().max()) > 0
 
 
+def test_two_caller_streams_with_small_and_tiled_matrices():
+    """Two shards stepped at the same time on two caller streams (own workspaces), each with
+    small matrices (on chip, on a side stream beside the tiled products) and tiled ones:
+    every result equals that shard stepped alone on the default stream, bit for bit."""
+    shapes = [(64, 64), (96, 128), (384, 1024), (300, 520)]
+    runs = {k: Run(shapes, R=1, seed=s_) for k, s_ in (("a", 71), ("b", 72), ("ra", 71), ("rb", 72))}
+    runs["ra"].step()
+    runs["rb"].step()
+    streams = {"a": torch.cuda.Stream(), "b": torch.cuda.Stream()}
+    for k in ("a", "b"):
+        r = runs[k]
+        nb = cz.cz_workspace_size(r.plan, 0, shapes)
+        r.WS = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+        r.opts = cz.make_opts(param_bf16=r.PB, debug_update_out=r.D, workspace=r.WS, workspace_bytes=nb)
+    torch.cuda.synchronize()
+    for _ in range(3):       # the first call builds each program; later ones overlap on the GPU
+        for k in ("a", "b"):
+            r = runs[k]
+            r.P.copy_(r.p0.cuda())
+            r.M.zero_()
+        torch.cuda.synchronize()
+        for k in ("a", "b"):
+            r = runs[k]
+            cz.cz_muon_step_ex(r.plan, 0, r.P, r.G, r.M, r.args, LR, MU, 5, streams[k], r.opts)
+        torch.cuda.synchronize()
+        for k, ref in (("a", "ra"), ("b", "rb")):
+            assert cz.cz_device_status(None, runs[k].WS) == cz.CZ_OK
+            for buf in ("P", "M", "PB", "D"):
+                assert torch.equal(getattr(runs[k], buf), getattr(runs[ref], buf)), (k, buf)
+
+
 SMALL_SHAPES = [(1, 5), (7, 1), (3, 256), (256, 128), (128, 256), (100, 130), (130, 100), (64, 64),
                 (128, 128), (17, 255), (33, 65), (96, 192)]
 

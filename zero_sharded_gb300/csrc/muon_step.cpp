@@ -763,19 +763,23 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   return CZ_OK;
 }
 
-// The library's side stream of the current device (non-blocking, never destroyed).
-cudaStream_t side_stream() {
-  static std::map<int, cudaStream_t> streams;   // callers hold g_mu
+// The library's side stream for the caller's stream `s` on the current device
+// (non-blocking, never destroyed).  One per caller stream: a side stream shared
+// by several caller streams would order their work behind one another and could
+// close a wait cycle that the caller's own event waits do not have.
+cudaStream_t side_stream(cudaStream_t s) {
+  static std::map<std::pair<int, cudaStream_t>, cudaStream_t> streams;   // callers hold g_mu
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  auto it = streams.find(dev);
+  const auto key = std::make_pair(dev, s);
+  auto it = streams.find(key);
   if (it != streams.end()) return it->second;
   cudaStream_t st = nullptr;
   if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
-  streams.emplace(dev, st);
+  streams.emplace(key, st);
   return st;
 }
 
@@ -970,7 +974,7 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
     SmallParams sp = P.small;
     sp.ns_steps = ns_steps;
     sp.a = opts->a; sp.b = opts->b; sp.c = opts->c; sp.lr = lr; sp.lr_dev = opts->lr_device;
-    cudaStream_t side = (P.fork_small && !capturing) ? side_stream() : nullptr;
+    cudaStream_t side = (P.fork_small && !capturing) ? side_stream(s) : nullptr;
     if (side) {
       if (cudaEventRecord(P.fork_ev, s) != cudaSuccess || cudaStreamWaitEvent(side, P.fork_ev, 0) != cudaSuccess)
         return CZ_ERR_CUDA;
