@@ -224,7 +224,12 @@ int cz_workspace_size(const cz_plan* plan, int32_t rank, const int64_t* shapes, 
  * returns CZ_ERR_INVALID before enqueuing anything.  The graph replays the
  * captured scalars (lr, mu, ...) and reads the buffers in place; the library
  * keeps the captured program's page-locked tables until the process exits.
- * Kernel timing (cz_profile_enable) skips captured launches. */
+ * Kernel timing (cz_profile_enable) skips captured launches.
+ * Streams: all work is ordered on `stream`; when a shard has both small
+ * matrices (m <= 128, n <= 256) and tiled ones, the small ones' launch may run
+ * on a library-owned side stream (one per caller stream, never destroyed) that
+ * is forked from `stream` after the momentum pass and joined back into it, so
+ * that work enqueued on `stream` after the call still follows all of the step. */
 int cz_muon_step(const cz_plan* plan, int32_t rank,
                  float* flat_param, const void* flat_grad, float* flat_mom,
                  const int64_t* offsets, const int64_t* shapes,
