@@ -528,6 +528,29 @@ def test_more_shape_groups_than_one_launch_holds():
     check_against_oracle(run, [True] * len(shapes), run.p0, run.m0)
 
 
+@pytest.mark.parametrize("ns_steps", [63, 64])
+def test_largest_step_counts(tmp_path, ns_steps):
+    """The largest accepted step counts (the fused launch's counters hold 64 steps): fused and
+    per-product launches bit for bit, results finite, and every update's singular values,
+    divided by lr * scale, inside the quintic map's band [0.5, 1.3].  After this many steps
+    the fp64 oracle is no reference: the band's fixed points repel (|f'| = 1.58 at 0.868 and
+    6.5 at 1.264), so rounding differences grow along each singular value's orbit."""
+    shapes = [(384, 1024), (1024, 384), (256, 256)]
+    run = Run(shapes, R=1, seed=23)
+    run.step(ns_steps=ns_steps)
+    D = run.D.cpu()
+    assert bool(torch.isfinite(D).all())
+    for i, (r, c) in enumerate(shapes):
+        sv = np.linalg.svd(run.tensor(D, i).numpy().astype(np.float64) / (LR * OM.shape_scale(r, c)),
+                           compute_uv=False)
+        assert 0.5 <= sv.min() and sv.max() <= 1.3, ((r, c), sv.min(), sv.max())
+    on = _run_child(tmp_path, "CZ_NS_FUSED", "1", shapes, ns_steps=ns_steps)
+    off = _run_child(tmp_path, "CZ_NS_FUSED", "0", shapes, ns_steps=ns_steps)
+    assert on["launches"]["ns_fused"] == 2 and off["launches"]["ns_fused"] == 0
+    assert torch.equal(on["P"], off["P"])
+    assert torch.equal(on["M"], off["M"])
+
+
 @pytest.mark.parametrize("ns_steps", [2, 6])
 def test_even_step_counts_end_in_the_other_x_buffer(tmp_path, ns_steps):
     """With an even number of Newton-Schulz steps the last Update (the apply) reads the second X ping-pong
