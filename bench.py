@@ -318,20 +318,28 @@ def torch_library_step(P, G, M, shapes, offsets, lr=LR, mu=MU, steps=NS_STEPS, c
             P[off:off + r * cc].view(r, cc).sub_((xk.t() if r > cc else xk), alpha=lr * max(1.0, r / cc) ** 0.5)
 
 
-def time_oracle_sample(shapes, grad_std, seed=0, max_per_shape=1):
-    """Times the fp64 oracle on one tensor of each distinct shape and extrapolates
-    to the whole shard by multiplicity.  Returns (ms_per_step, sample_desc, cores)."""
+ORACLE_WHOLE_FLOPS = 3e12   # shards up to this much Newton-Schulz work are timed whole (about 10 s of fp64)
+
+
+def time_oracle_sample(shapes, grad_std, seed=0):
+    """Times the fp64 oracle over the shard: every tensor when its Newton-Schulz work is
+    at most ORACLE_WHOLE_FLOPS (the tiny workload and the Qwen3-1.7B layer), else one
+    tensor of each distinct shape, extrapolated by multiplicity.
+    Returns (ms_per_step, sample_desc, cores)."""
     import numpy as np
 
     from oracle import muon as OM
 
+    flops = sum(NS_STEPS * (4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3) for r, c in shapes)
+    whole = flops <= ORACLE_WHOLE_FLOPS
     distinct = {}
     for s in shapes:
         distinct[s] = distinct.get(s, 0) + 1
+    todo = [(s, 1) for s in shapes] if whole else list(distinct.items())
     rng = np.random.default_rng(seed)
     total_ms = 0.0
     parts = []
-    for (r, c), mult in distinct.items():
+    for (r, c), mult in todo:
         W = (0.02 * rng.standard_normal((r, c))).astype(np.float32)
         g = (grad_std * rng.standard_normal((r, c))).astype(np.float32)
         m = np.zeros((r, c), np.float32)
@@ -340,8 +348,11 @@ def time_oracle_sample(shapes, grad_std, seed=0, max_per_shape=1):
         dt = (time.perf_counter() - t0) * 1e3
         total_ms += dt * mult
         parts.append(f"{r}x{c}")
-    desc = (f"oracle (fp64 NumPy) on one tensor of each distinct shape ({', '.join(parts)}; "
-            f"{len(distinct)} of {len(shapes)} tensors), extrapolated by multiplicity")
+    if whole:
+        desc = f"oracle (fp64 NumPy) on every tensor of the shard ({len(shapes)} tensors), timed whole"
+    else:
+        desc = (f"oracle (fp64 NumPy) on one tensor of each distinct shape ({', '.join(parts)}; "
+                f"{len(distinct)} of {len(shapes)} tensors), extrapolated by multiplicity")
     return total_ms, desc, os.cpu_count() or 1
 
 
