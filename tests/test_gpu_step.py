@@ -512,6 +512,52 @@ def test_low_rank_plus_noise_gradients_track_the_rounding_model():
     check_against_oracle(run, [True] * len(shapes), run.p0, run.m0, tol=tols)
 
 
+def test_degenerate_gradients_zero_and_rank_one():
+    """A zero gradient (with zero momentum) leaves its tensor exactly unchanged: u = 0, X0 = 0 / (0 + eps) = 0,
+    and the iteration keeps X = 0. An exactly rank-one gradient s u v^T: in exact arithmetic the update is
+    lr * scale * f^5(1) u v^T (f^5(1) = 0.6964364). In bf16 the rounding of X0 puts singular values of order
+    2^-9 beside the rank-one direction, which f^5 amplifies by up to a^5 ~ 485, so the update lands far from
+    the closed form in Frobenius norm: the NumPy rounding model lands about 1.17 away. Held to: the component
+    along u v^T within 1e-2 of f^5(1), every singular value of update / (lr * scale) in f's range (<= 1.3),
+    and the Frobenius distance within 1.5x the rounding model's. Tiled wide, tall and square tensors, plus
+    small ones on chip."""
+    from tests.bf16_model import orthogonalise_bf16
+    shapes = [(256, 640), (640, 256), (384, 384), (64, 96), (96, 64), (128, 256)]
+    zero = {2, 5}
+    run = Run(shapes, R=1, seed=29)
+    rng = np.random.default_rng(29)
+    g = torch.zeros_like(run.g)
+    uv = {}
+    for i, (r, c) in enumerate(shapes):
+        if i in zero:
+            continue
+        u = rng.standard_normal(r); u /= np.linalg.norm(u)
+        v = rng.standard_normal(c); v /= np.linalg.norm(v)
+        uv[i] = np.outer(u, v)
+        o = run.offsets[i]
+        g[o:o + r * c] = torch.from_numpy((2.5 * uv[i]).astype(np.float32).reshape(-1))
+    run.g = g
+    run.G = g.cuda()
+    run.step()
+    P, M, D, PB = run.P.cpu(), run.M.cpu(), run.D.cpu(), run.PB.cpu()
+    f5 = OM.ns_poly_scalar(1.0)
+    for i, (r, c) in enumerate(shapes):
+        if i in zero:
+            assert torch.equal(run.tensor(P, i), run.tensor(run.p0, i))
+            assert not bool(run.tensor(M, i).any()) and not bool(run.tensor(D, i).any())
+            assert torch.equal(run.tensor(PB, i), run.tensor(run.p0, i).to(torch.bfloat16))
+            continue
+        x = run.tensor(D, i).numpy().astype(np.float64) / (LR * OM.shape_scale(r, c))
+        assert abs(float(np.sum(x * uv[i])) - f5) <= 1e-2, (r, c)
+        assert np.linalg.svd(x, compute_uv=False).max() <= 1.3, (r, c)
+        _, u_in = OM.momentum(run.tensor(run.g, i).numpy(), np.zeros((r, c), np.float32), MU)
+        exact = OM.orthogonalise(u_in, 5)
+        e_model = rel_fro(orthogonalise_bf16(u_in, 5), exact)
+        assert rel_fro(x, exact) <= 1.5 * e_model, (r, c)
+        # the master moved by exactly the reported delta
+        assert torch.equal(run.tensor(P, i), run.tensor(run.p0, i) - run.tensor(D, i))
+
+
 def test_more_shape_groups_than_one_launch_holds():
     """40 distinct tiled shapes (a launch's problem table holds 32 groups): every Newton-Schulz product runs as
     two launches over the groups, the fused launch steps aside, and every tensor still matches the oracle."""
