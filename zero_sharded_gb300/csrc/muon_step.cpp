@@ -422,9 +422,12 @@ void grouped_tiles(std::vector<int4>& out, int mat, int64_t TM, int64_t TN, bool
   }
 }
 
+// carry: null, or per-unit loads that the assignment starts from and adds to (a
+// list that fits one launch only), so that consecutive lists balance their sum.
 bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int4* host_tiles, int64_t& tile_cursor,
                    int32_t* dev_cta, int32_t* host_cta, int64_t& cta_cursor, int max_grid, const GemmParams& common,
-                   std::vector<Launch>& out, int first, int cur) {
+                   std::vector<Launch>& out, int first, int cur, std::vector<int64_t>* carry) {
+  if (carry && probs.size() > (size_t)kMaxProblems) carry = nullptr;
   for (size_t c0 = 0; c0 < probs.size(); c0 += kMaxProblems) {
     const size_t c1 = std::min(probs.size(), c0 + (size_t)kMaxProblems);
     std::vector<TileRef> tl;
@@ -440,7 +443,8 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
     {
       // min-heap of (load, cta)
       std::vector<std::pair<int64_t, int>> heap;
-      for (int b = 0; b < grid; ++b) heap.push_back({0, b});
+      if (carry) carry->resize((size_t)grid, 0);
+      for (int b = 0; b < grid; ++b) heap.push_back({carry ? (*carry)[(size_t)b] : 0, b});
       auto gt = [](const std::pair<int64_t, int>& x, const std::pair<int64_t, int>& y) { return x > y; };
       std::make_heap(heap.begin(), heap.end(), gt);
       for (const TileRef& r : tl) {
@@ -450,6 +454,8 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
         top.first += r.cost;
         std::push_heap(heap.begin(), heap.end(), gt);
       }
+      if (carry)
+        for (const auto& e : heap) (*carry)[(size_t)e.second] = e.first;
     }
     Launch ln;
     ln.phase = phase;
@@ -665,16 +671,37 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   }
   const int units = (int)std::min<int64_t>(max_grid, most);
   // Gram with first=0/1 share one tile list: build first, copy for the other flag.
-  auto ml = [&](int phase, std::vector<ProbDesc>& probs, std::vector<Launch>& out, int cur) {
+  auto ml = [&](int phase, std::vector<ProbDesc>& probs, std::vector<Launch>& out, int cur,
+                std::vector<int64_t>* carry) {
     make_launches(phase, probs, dev_tiles, host_tiles, cursor, dev_cta, host_cta, cta_cursor, units, common, out,
-                  0, cur);
+                  0, cur, carry);
   };
-  ml(kGram, gram[0], P.gram[0], 0);
-  ml(kGram, gram[1], P.gram[1], 1);
-  ml(kPoly, poly, P.poly, 0);
+  // The fused launch walks a step's Gram, Poly and Update (or Apply) lists on every
+  // unit, so when it will run, each list's assignment starts from the loads the
+  // previous list left: the units' totals per step are balanced, not each list
+  // alone (balancing each alone leaves the same low-index units heavier in every
+  // list, since ties go to the lower index).  One launch per product keeps each
+  // list balanced on its own.
+  bool fused_candidate = use_fused();
+  {
+    int64_t xb = 0;
+    for (const Group& G : L.groups)
+      if (!G.small) xb += 2 * (int64_t)G.m * G.n * G.count;
+    size_t np = 0;
+    for (auto* v : {&gram[0], &gram[1], &poly, &upd[0], &upd[1], &app[0], &app[1]}) np += v->size();
+    fused_candidate = fused_candidate && np <= (size_t)kMaxProblems && xb <= l2_bytes();
+  }
+  std::vector<int64_t> c_gram, c_poly;
+  std::vector<int64_t>* cg = fused_candidate ? &c_gram : nullptr;
+  ml(kGram, gram[0], P.gram[0], 0, cg);
+  c_poly = c_gram;                 // the Poly list starts where Gram left the units
+  if (cg) c_gram.assign(c_gram.size(), 0);
+  ml(kGram, gram[1], P.gram[1], 1, cg);   // the same tiles from the same start: the same assignment
+  ml(kPoly, poly, P.poly, 0, fused_candidate ? &c_poly : nullptr);
   for (int cur = 0; cur < 2; ++cur) {
-    ml(kUpdate, upd[cur], P.update[cur], cur);
-    ml(kApply, app[cur], P.apply[cur], cur);
+    std::vector<int64_t> cu = c_poly, ca = c_poly;
+    ml(kUpdate, upd[cur], P.update[cur], cur, fused_candidate ? &cu : nullptr);
+    ml(kApply, app[cur], P.apply[cur], cur, fused_candidate ? &ca : nullptr);
   }
   (void)ns_steps;
   SmallParams& sp = P.small;
