@@ -98,10 +98,10 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("cd2b602c9175f148", {"qwen3-1.7b-layer": {"ns_fused": 2593.78e6, "ns_gram": 125.07e6, "ns_poly": 50.86e6,
+    "ns_gemm": ("d23fd3ed8cef9f2d", {"qwen3-1.7b-layer": {"ns_fused": 2593.78e6, "ns_gram": 125.07e6, "ns_poly": 50.86e6,
                                                     "ns_update": 217.02e6, "ns_update_apply": 620.39e6}}),
-    "momentum": ("765bfd301a49ec31", {"qwen3-1.7b-layer": {"momentum": 646.05e6}}),
-    "ns_small": ("cd66867d40c17170", {"tiny": {"ns_small": 0.3425e6}}),
+    "momentum": ("9b27a7e80286966e", {"qwen3-1.7b-layer": {"momentum": 646.05e6}}),
+    "ns_small": ("5decde10087a6d19", {"tiny": {"ns_small": 0.3425e6}}),
     "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 

@@ -70,7 +70,7 @@ struct Layout {
   int64_t off_cta = 0;             // per launch: grid+1 tile offsets (int32)
   int64_t n_cta_entries = 0;
   int64_t off_expect = 0;          // fused launch: n_mats x 3 expected arrivals (int32)
-  int64_t off_done = 0;            // fused launch: 3 x kMaxNsSteps x n_mats counters (int32)
+  int64_t off_done = 0;            // fused launch: 3 x kMaxNsSteps x n_mats counters (int32), zero in the tables
   int64_t bytes = 0;
 };
 
@@ -177,7 +177,7 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   L.off_expect = off; off = align_up(off + 4 * 3 * std::max<int64_t>(n_mats, 1), kAlign);
   L.off_done = off; off = align_up(off + 4 * 3 * kMaxNsSteps * std::max<int64_t>(n_mats, 1), kAlign);
   // per-tile partial sums of the momentum pass: written before they are read, so outside the tables
-  // that are uploaded on every call
+  // that are copied in on every call
   L.off_partial = off; off = align_up(off + 4 * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
   for (Group& G : L.groups) {
     G.ldx = align_up(G.n, 8);
