@@ -9,6 +9,7 @@ import random
 import re
 
 import pytest
+import torch
 
 from oracle import planner as O
 from zero_sharded_gb300 import cz
@@ -146,6 +147,30 @@ def test_workspace_size_grows_with_shard():
     approx = sum(4 * r * c + 4 * min(r, c) ** 2 for r, c in w.shapes)
     assert approx <= s1 <= approx * 1.05
     assert s2 >= s1 * 0.95
+
+
+def test_bucket_pack_validation_before_any_gpu_work():
+    """cz_bucket_pack / cz_bucket_unpack reject bad layouts on the host (never touching the buffers, which are
+    host tensors standing in for device ones); a zero-sized block is a no-op."""
+    import ctypes
+    lib = cz.load()
+    b = torch.zeros(10)
+    p = torch.zeros(20)
+    bad = [([1, 10], 10), ([0, 6, 4], 10), ([0, 6, 10], 5), ([0, 10], -1)]
+    for cuts, block in bad:
+        for fn in (cz.cz_bucket_pack, cz.cz_bucket_unpack):
+            with pytest.raises(cz.CzError) as e:
+                fn(b, cuts, block, p)
+            assert e.value.status == cz.CZ_ERR_INVALID
+    cut_arr = (ctypes.c_int64 * 2)(0, 10)
+    for elem_bytes in (0, 3, 16):
+        assert lib.cz_bucket_pack(b.data_ptr(), elem_bytes, cut_arr, 1, 10, p.data_ptr(), None) == cz.CZ_ERR_INVALID
+    assert lib.cz_bucket_pack(None, 4, cut_arr, 1, 10, p.data_ptr(), None) == cz.CZ_ERR_INVALID
+    assert lib.cz_bucket_unpack(p.data_ptr(), 4, cut_arr, 1, 10, None, None) == cz.CZ_ERR_INVALID
+    many = (ctypes.c_int64 * 1026)(*([0] * 1026))
+    assert lib.cz_bucket_pack(b.data_ptr(), 4, many, 1025, 0, p.data_ptr(), None) == cz.CZ_ERR_INVALID  # > 1024 ranks
+    empty = (ctypes.c_int64 * 3)(0, 0, 0)
+    assert lib.cz_bucket_pack(b.data_ptr(), 4, empty, 2, 0, p.data_ptr(), None) == cz.CZ_OK      # nothing to move
 
 
 def test_apply_validation_before_any_gpu_work():
