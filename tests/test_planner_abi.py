@@ -203,5 +203,9 @@ def test_empty_shard_is_a_no_op_without_a_device():
     empty = [r for r in range(4) if r not in owner]
     assert empty
     fake = 0x1000
+    built = cz.cz_step_programs_built()
     for r in empty:
         cz.cz_muon_step(p, r, fake, fake, fake, cz.StepArgs([0, 4096], shapes), 0.02, 0.95, 5)
+    with pytest.raises(cz.CzError):                     # rejected on the host: nothing is built either
+        cz.cz_muon_step(p, 0, fake + 4, fake, fake, cz.StepArgs([0, 4096], shapes), 0.02, 0.95, 5)
+    assert cz.cz_step_programs_built() == built
