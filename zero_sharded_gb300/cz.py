@@ -317,6 +317,10 @@ def cz_muon_step_noalloc(plan: Plan, rank: int, flat_param, flat_grad, flat_mom,
 def make_opts(param_bf16=None, workspace=None, workspace_bytes: int = 0, debug_update_out=None,
               grad_is_bf16: bool = False, nesterov: bool = True, eps: Optional[float] = None,
               coeffs: Optional[Tuple[float, float, float]] = None, lr_device=None) -> cz_step_opts:
+    """cz_step_opts from the library defaults with the given overrides (tensors are passed by
+    data pointer): bf16 parameter copy, caller workspace, debug delta, bf16 gradients, Nesterov,
+    eps, Newton-Schulz coefficients (a, b, c), and lr_device, a one-element fp32 device tensor
+    read in place of the lr argument (for a learning-rate schedule under a CUDA graph)."""
     o = cz_step_opts_default()
     o.lr_device = _ptr(lr_device)
     o.param_bf16 = _ptr(param_bf16)
