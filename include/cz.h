@@ -251,21 +251,29 @@ int cz_step_programs_built(int64_t* count);
  * to this call; it exists for callers that cannot call cudaMalloc when they run
  * the step (an allocator that owns all device memory, memory reserved up front,
  * or code that must avoid the synchronisation cudaMalloc/cudaFree can cause).
- * Same arguments, kernels and results as cz_muon_step_ex; the workspace is a
- * static device array of CZ_STATIC_WORKSPACE_BYTES (64 MiB) that every GPU
- * loading the library holds until the process exits.
+ * Same arguments, kernels and results as cz_muon_step_ex (bit for bit, for the
+ * same inputs); the workspace is a static device array of
+ * CZ_STATIC_WORKSPACE_BYTES (64 MiB) that every GPU loading it holds until the
+ * process exits.
  *   - opts may be NULL (defaults); opts->workspace must be NULL and
  *     workspace_bytes 0, else CZ_ERR_INVALID.
  *   - A shard whose cz_workspace_size exceeds CZ_STATIC_WORKSPACE_BYTES is
  *     rejected with CZ_ERR_NOMEM before any GPU work.
- *   - The first call on each device does a set-up (looks up the array's device
- *     address and clears its status word, synchronously).
- *   - All calls share the one array: calls that overlap on the GPU (other
- *     streams, other threads) race.  Device-side errors are recorded in the
- *     array's status word and are not reported by this call.
- * Calls no cudaMalloc, cudaFree or other allocating routine, and page-locks no
- * host memory: its launch tables are uploaded from pageable memory, so it cannot
- * be captured into a CUDA graph (CZ_ERR_INVALID inside a capture). */
+ *   - The first call on each device does a set-up: it looks up the array's
+ *     device address and clears the array's status word on `stream`.  Under
+ *     lazy module loading (the CUDA default) that look-up is also when the
+ *     runtime loads the array, so the driver reserves its 64 MiB in this first
+ *     call, which can fail with CZ_ERR_CUDA when device memory is exhausted.
+ *     Make the first call on a device before any stream capture.  Later calls
+ *     allocate nothing.
+ *   - All calls share the one array, which keeps the previous call's contents
+ *     (each call re-uploads its tables and overwrites what its kernels read):
+ *     calls that overlap on the GPU (other streams, other threads) race.
+ *   - Device-side errors go to the array's status word; cz_device_status with a
+ *     NULL workspace reads and clears it.
+ * Calls no cudaMalloc, cudaFree or other allocating routine and page-locks no
+ * host memory: its launch tables are uploaded from pageable memory by
+ * cudaMemcpyAsync. */
 #define CZ_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
 int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank,
                          float* flat_param, const void* flat_grad, float* flat_mom,
@@ -274,8 +282,12 @@ int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank,
                          const cz_step_opts* opts);
 
 /* Synchronises `stream`, reads and clears the device status word kept in
- * `workspace` (NULL: the library's cached workspace of the current device).
- * *status_out = CZ_OK or the first CZ_ERR_* a kernel recorded. */
+ * `workspace`.  NULL reads and clears every library-owned scratch of the current
+ * device that exists: the cached workspace of cz_muon_step(_ex) and the static
+ * array of cz_muon_step_noalloc.  *status_out = CZ_OK or the first CZ_ERR_* a
+ * kernel recorded (with NULL: the cached workspace's first).  The `workspace`
+ * argument is an addition to the pages-derived boundary: the caller owns the
+ * workspace that holds its status word, so the call must be told which one. */
 int cz_device_status(void* stream, void* workspace, int* status_out);
 
 /* Kernel timing (tracing).  While enabled, every kernel that cz_muon_step(_ex)

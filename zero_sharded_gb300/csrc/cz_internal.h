@@ -55,4 +55,9 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
               const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps, void* stream,
               const cz_step_opts* opts, bool pin_ok);
 
+// Device address of cz_muon_step_noalloc's static scratch on the current device,
+// or null if no such call has set it up there; cz_device_status(stream, NULL)
+// reads and clears its status word.
+void* noalloc_scratch_if_set_up();
+
 }  // namespace cz

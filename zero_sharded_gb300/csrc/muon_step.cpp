@@ -1081,19 +1081,25 @@ int cz_device_status(void* stream, void* workspace, int* status_out) {
   *status_out = CZ_OK;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CZ_ERR_CUDA;
-  void* ws = workspace;
-  if (!ws) {
+  // the status words to read: the caller's workspace, or every library-owned
+  // scratch of the current device (the cached workspace of cz_muon_step(_ex) and
+  // the static array of cz_muon_step_noalloc, where each has been set up)
+  void* words[2] = {workspace, nullptr};
+  if (!workspace) {
     std::lock_guard<std::mutex> lock(g_mu);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CZ_ERR_CUDA;
     auto it = g_ws.find(dev);
-    if (it == g_ws.end() || !it->second.ptr) return CZ_OK;
-    ws = it->second.ptr;
+    words[0] = (it == g_ws.end()) ? nullptr : it->second.ptr;
+    words[1] = noalloc_scratch_if_set_up();
   }
-  int v = 0;
-  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CZ_ERR_CUDA;
-  if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return CZ_ERR_CUDA;
-  *status_out = v;
+  for (void* ws : words) {
+    if (!ws) continue;
+    int v = 0;
+    if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return CZ_ERR_CUDA;
+    if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return CZ_ERR_CUDA;
+    if (*status_out == CZ_OK) *status_out = v;   // the first error found is reported; every word is cleared
+  }
   return CZ_OK;
 }
 

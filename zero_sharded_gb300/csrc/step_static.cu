@@ -9,12 +9,16 @@
 // the workspace is the file-scope array below, so the call allocates nothing:
 // no cudaMalloc, no cudaFree, no allocating library routine.
 //
-// The array holds CZ_STATIC_WORKSPACE_BYTES on every GPU that loads the library,
-// for the life of the process.  Every call shares it and it keeps the previous
-// call's contents: the kernels overwrite everything they read except the status
-// word, which is cleared once per device at set-up.  Calls that overlap on the
-// GPU (different streams, or different host threads without ordering) race on
-// the array.
+// The array holds CZ_STATIC_WORKSPACE_BYTES on every GPU that loads it, for the
+// life of the process.  The CUDA runtime loads this file's module (and with it
+// the array) when the module is first used on a device; under lazy module
+// loading, the default, that is the first call's address look-up, so the first
+// call on each device is where the driver reserves the array's memory.  Every
+// call shares the array and it keeps the previous call's contents: the kernels
+// overwrite everything they read except the status word, which the first call on
+// a device clears on the caller's stream and cz_device_status(stream, NULL)
+// reads and clears afterwards.  Calls that overlap on the GPU (different streams,
+// or different host threads without ordering) race on the array.
 
 #include <cuda_runtime.h>
 
@@ -33,8 +37,10 @@ std::map<int, void*> g_noalloc_ptr;   // per device: device address of g_noalloc
 
 // Set-up, once per device, with that device current: the host name of the
 // array is only a stand-in, so its device address is looked up here and passed
-// on as the workspace pointer.
-int noalloc_scratch(void** out) {
+// on as the workspace pointer.  The status word (the first bytes of the
+// workspace header) is cleared on the caller's stream, ahead of the first step's
+// kernels on that stream.
+int noalloc_scratch(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CZ_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
@@ -46,8 +52,10 @@ int noalloc_scratch(void** out) {
       cudaGetLastError();
       return CZ_ERR_CUDA;
     }
-    // the status word (first bytes of the workspace header) must start at zero
-    if (cudaMemset(ptr, 0, 256) != cudaSuccess) return CZ_ERR_CUDA;
+    if (cudaMemsetAsync(ptr, 0, 256, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return CZ_ERR_CUDA;
+    }
     it = g_noalloc_ptr.emplace(dev, ptr).first;
   }
   *out = it->second;
@@ -55,6 +63,24 @@ int noalloc_scratch(void** out) {
 }
 
 }  // namespace
+
+namespace cz {
+
+// The array's device address on the current device, or null if no
+// cz_muon_step_noalloc call has set it up there (nothing is looked up or
+// loaded here).
+void* noalloc_scratch_if_set_up() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  auto it = g_noalloc_ptr.find(dev);
+  return it == g_noalloc_ptr.end() ? nullptr : it->second;
+}
+
+}  // namespace cz
 
 extern "C" int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank, float* flat_param, const void* flat_grad,
                                     float* flat_mom, const int64_t* offsets, const int64_t* shapes, float lr,
@@ -80,7 +106,7 @@ extern "C" int cz_muon_step_noalloc(const cz_plan* plan, int32_t rank, float* fl
   if (st != CZ_OK) return st;
   if (need > (size_t)CZ_STATIC_WORKSPACE_BYTES) return CZ_ERR_NOMEM;   // shard too large for the array
   void* scratch = nullptr;
-  st = noalloc_scratch(&scratch);
+  st = noalloc_scratch(reinterpret_cast<cudaStream_t>(stream), &scratch);
   if (st != CZ_OK) return st;
   o.workspace = scratch;
   o.workspace_bytes = (size_t)CZ_STATIC_WORKSPACE_BYTES;
