@@ -72,9 +72,10 @@ def test_qwen3_14b_microgroup_full_size():
     first = {}
     for i, s in enumerate(w.shapes):
         first.setdefault(s, i)
-    # k/v (1024x5120), q/o (5120x5120), down (5120x17408); gate/up (tall) share the down group's kernels
-    sample = [first[s] for s in [(1024, 5120), (5120, 5120), (5120, 17408)] if s in first]
-    assert len(sample) >= 2
+    # k/v (1024x5120), q/o (5120x5120), down (5120x17408, wide) and gate/up (17408x5120, tall: the
+    # transposed apply), each the first of its shape in the draw
+    sample = [first[s] for s in [(1024, 5120), (5120, 5120), (5120, 17408), (17408, 5120)] if s in first]
+    assert (5120, 17408) in first and (17408, 5120) in first
     _run_full(w, sample)
 
 
@@ -104,8 +105,9 @@ def test_qwen3_32b_heaviest_shard_full_size():
     w = wl.Workload("shard", shapes, names, 0.02, 1e-3)
     tall = [i for i, (r, c) in enumerate(shapes) if r > c]
     wide = [i for i, (r, c) in enumerate(shapes) if r <= c]
-    sample = (tall[:1] or wide[:1])
-    _run_full(w, sample)
+    # gate/up (25600x5120) take the transposed apply, down (5120x25600) the direct one: one of each
+    assert tall and wide
+    _run_full(w, [tall[0], wide[0]])
 
 
 def test_bounded_wait_times_out_and_context_stays_usable():
