@@ -1,15 +1,26 @@
 #!/usr/bin/env python
 """Bench of the local Muon step one data-parallel rank runs on its shard.
 
-Default workload: one Qwen3-1.7B-shaped layer (q 2048x2048, k/v 1024x2048,
-o 2048x2048, gate/up 6144x2048, down 2048x6144; 50,331,648 elements), fp32
-master/momentum/gradients, bf16 parameter copy, mu=0.95 Nesterov, lr=0.02,
-5 quintic Newton-Schulz steps.  Under torchrun with N ranks the job is N such
-layers partitioned by the alpha-Balanced planner (R=N, alpha=1); each rank steps
-its own shard with no collective inside the step (weak scaling).
+Default workload: the heaviest rank's shard of a Qwen3-32B-shaped model (64
+layers laid out in reverse layer order in 40,000,000-element buckets, planned by
+the alpha-Balanced Greedy LPT planner with R = 32, alpha = 1, cost = numel): 8
+FFN matrices of 5120 x 25600 (gate/up 25600 x 5120, down 5120 x 25600),
+1,048,576,000 elements, fp32 master/momentum/gradients, bf16 parameter copy,
+mu = 0.95 Nesterov, lr = 0.02, 5 quintic Newton-Schulz steps.  Other workloads:
+`--workload` (the tiny six-matrix case, one Qwen3-1.7B-shaped layer, 28 such
+layers, the 64-matrix Qwen3-14B micro-group, and the shards of the FLOPs-cost
+comparison).  Under torchrun with N ranks each GPU steps its own shard (the k-th
+heaviest of the R = 32 plan for the Qwen3-32B shard; a layer of N layers planned
+with R = N otherwise) with no collective inside the step (weak scaling).
 
-Prints ONE JSON line (rank 0).  `value` is milliseconds per shard-step for the
-whole job: the slowest rank's mean step time divided by the number of shards.
+Prints ONE JSON line (rank 0).  `value` is the slowest rank's mean step time in
+milliseconds (weak scaling: a flat value over N is perfect scaling);
+`ms_per_shard_job` divides it by the number of shards.
+
+`--compare-cost` instead times every distinct shard of the Qwen3-32B layout under
+the numel-cost plan and under the Newton-Schulz-FLOPs-cost plan and prints one
+JSON line with each plan's slowest shard (the step is communication-free, so the
+slowest shard sets the distributed optimizer step).
 """
 
 from __future__ import annotations
@@ -84,6 +95,26 @@ def ns_flops_executed(shapes, steps=NS_STEPS, bn=256):
     return tot
 
 
+def ns_flops_executed_by_kind(shapes, steps=NS_STEPS, bn=256):
+    """Executed flops per step of each GEMM kernel kind, counted as ns_flops_executed counts them."""
+    bm = 128 if os.environ.get("CZ_NS_PAIR", "1") == "0" else 256
+
+    def cdiv(a, b):
+        return (a + b - 1) // b
+    g = p = u = 0
+    for r, c in shapes:
+        if _is_small(r, c):
+            continue
+        m, n = min(r, c), max(r, c)
+        sym = sum(1 for a in range(cdiv(m, bm)) for b in range(cdiv(m, bn)) if a * bm <= b * bn + bn - 1)
+        g += sym * 2 * bm * bn * cdiv(n, 64) * 64
+        p += sym * 2 * bm * bn * cdiv(m, 64) * 64
+        u += cdiv(m, bm) * cdiv(n, bn) * 2 * bm * bn * cdiv(m, 64) * 64
+    small = ns_flops_executed([s for s in shapes if _is_small(*s)], steps)
+    return {"ns_gram": steps * g, "ns_poly": steps * p, "ns_update": (steps - 1) * u, "ns_update_apply": u,
+            "ns_fused": steps * (g + p + u), "ns_small": small}
+
+
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures summarised
 # under profiles/, per kernel kind, keyed by a hash of the sources that kernel is built and launched from:
 # once one of them changes the figure no longer describes the kernel and the bench reports null.
@@ -139,39 +170,107 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------ workloads
-def build_workload(name: str, world: int, rank: int):
-    """Returns (shapes, numels, offsets, buckets, R, alpha, grad_bf16, grad_std, rank_to_run, desc)."""
+WORKLOADS = ["qwen3-32b-shard", "qwen3-1.7b-layer", "tiny", "qwen3-1.7b-28L", "qwen3-14b-microgroup",
+             "qwen3-32b-shard-flops", "qwen3-32b-shard-numel-maxflops", "qwen3-32b-ffn-pair"]
+DEFAULT_WORKLOAD = "qwen3-32b-shard"
+QWEN32_LAYOUT = "qwen3-32b 64 layers in reverse layer order, 448 tensors, 320 buckets of >= 40M elements"
+
+
+def plan_owner_load(numels, buckets, R, alpha, costs=None, planner="cz"):
+    """Algorithm 1's owner per tensor and load per rank.  The GPU arm plans through libcz; the reference
+    arm, which runs no code of the CUDA library, through the oracle's planner (bit-exact with libcz's)."""
+    if planner == "oracle":
+        from oracle import planner as OP
+
+        p = OP.plan_partition(numels, buckets, R, alpha, costs)
+        return list(p.owner), list(p.rank_load)
     from zero_sharded_gb300 import cz
+
+    if costs is None:
+        p = cz.cz_plan_partition(numels, buckets, R, alpha)
+    else:
+        p = cz.cz_plan_partition_cost(numels, costs, buckets, R, alpha)
+    return p.owner(), p.rank_load()
+
+
+def make_buckets(numels, cap, planner="cz"):
+    if planner == "oracle":
+        from oracle import planner as OP
+
+        return OP.make_buckets(numels, cap)
+    from zero_sharded_gb300 import cz
+
+    return cz.cz_make_buckets(numels, cap)
+
+
+def qwen32_plan(cost: str, planner="cz"):
+    """The 64-layer Qwen3-32B layout planned by Algorithm 1 (R = 32, alpha = 1) with W(p) = numel ("numel")
+    or W(p) = the tensor's Newton-Schulz flops K(4m^2n + 2m^3) ("flops").  Returns (layout, owner, load)."""
+    from zero_sharded_gb300 import workloads as wl
+
+    full = wl.qwen3_32b_reverse()
+    b = make_buckets(full.numels, full.bucket_cap, planner)
+    costs = None if cost == "numel" else [ns_flops([s]) for s in full.shapes]
+    own, load = plan_owner_load(full.numels, b, full.R, full.alpha, costs, planner)
+    return full, own, load
+
+
+def shard_of(full, owner, r: int, name: str):
+    """Plan rank r's tensors of the layout, in buffer order, as a workload of their own."""
+    from zero_sharded_gb300 import workloads as wl
+
+    shapes = [s for s, o in zip(full.shapes, owner) if o == r]
+    names = [n for n, o in zip(full.names, owner) if o == r]
+    return wl.Workload(name, shapes, names, full.param_std, full.grad_std)
+
+
+def build_workload(name: str, world: int, rank: int, planner="cz"):
+    """Returns (workload, buckets, R, alpha, plan rank this GPU runs, config extras)."""
     from zero_sharded_gb300 import workloads as wl
 
     if name == "qwen3-1.7b-layer":
         w = wl.qwen3_1p7b_layers(world)
-        buckets = cz.cz_make_buckets(w.numels, BUCKET_CAP) if world > 1 else [len(w.numels)]
-        return w, buckets, world, 1.0, rank
+        buckets = make_buckets(w.numels, BUCKET_CAP, planner) if world > 1 else [len(w.numels)]
+        return w, buckets, world, 1.0, rank, {"R": world, "alpha": 1.0}
     if name == "tiny":
         # one copy of the six tiny matrices per rank, one bucket per copy, planned with R = world
         base = wl.tiny()
         w = wl.Workload("tiny-6" if world == 1 else f"tiny-6x{world}", base.shapes * world,
                         [f"r{k}.{n}" for k in range(world) for n in base.names], base.param_std, base.grad_std)
-        return w, [len(base.shapes)] * world, world, 1.0, rank
+        return w, [len(base.shapes)] * world, world, 1.0, rank, {"R": world, "alpha": 1.0}
+    if name == "qwen3-32b-ffn-pair":
+        # one up (25600 x 5120, tall) and one down (5120 x 25600, wide) matrix of the Qwen3-32B shard: the
+        # headline shard's kernels at its shapes on a few GB of device memory (profiling captures)
+        w = wl.Workload("qwen3-32b-ffn-pair", [(25600, 5120), (5120, 25600)], ["up", "down"], 0.02, 1e-3)
+        return w, [2], 1, 1.0, 0, {"R": 1, "alpha": 1.0}
     if name == "qwen3-1.7b-28L":
         w = wl.qwen3_1p7b_layers(28)
-        return w, [len(w.numels)], 1, 1.0, 0
+        return w, [len(w.numels)], 1, 1.0, 0, {"R": 1, "alpha": 1.0}
     if name == "qwen3-14b-microgroup":
         w = wl.qwen3_14b_microgroup(64)
-        return w, [len(w.numels)], 1, 1.0, 0
-    if name == "qwen3-32b-shard":
-        # plan the whole 64-layer model, then run the heaviest rank's tensors
-        full = wl.qwen3_32b_reverse()
-        b = cz.cz_make_buckets(full.numels, full.bucket_cap)
-        plan = cz.cz_plan_partition(full.numels, b, full.R, full.alpha)
-        loads = plan.rank_load()
-        heavy = max(range(len(loads)), key=lambda r: loads[r])
-        own = plan.owner()
-        shapes = [s for s, o in zip(full.shapes, own) if o == heavy]
-        w = wl.Workload(f"qwen3-32b-R32-shard{heavy}", shapes, [n for n, o in zip(full.names, own) if o == heavy],
-                        0.02, 1e-3)
-        return w, [len(shapes)], 1, 1.0, 0
+        return w, [len(w.numels)], 1, 1.0, 0, {"R": 1, "alpha": 1.0}
+    if name in ("qwen3-32b-shard", "qwen3-32b-shard-flops", "qwen3-32b-shard-numel-maxflops"):
+        # plan the whole 64-layer model with R = 32, then run one rank's tensors on this GPU
+        cost = "flops" if name == "qwen3-32b-shard-flops" else "numel"
+        full, own, plan_load = qwen32_plan(cost, planner)
+        if name == "qwen3-32b-shard-numel-maxflops":
+            # the numel plan's rank with the most Newton-Schulz flops (its slowest rank)
+            fl = [0] * full.R
+            for s, o in zip(full.shapes, own):
+                fl[o] += ns_flops([s])
+            load, what = fl, "the most Newton-Schulz flops under the numel plan"
+        else:
+            load = plan_load
+            what = "the heaviest planned load" + (" (cost = Newton-Schulz flops)" if cost == "flops" else "")
+        order = sorted(range(full.R), key=lambda r: (-load[r], r))
+        r = order[rank % full.R]        # GPU rank k runs the k-th heaviest plan rank
+        tag = {"qwen3-32b-shard": "", "qwen3-32b-shard-flops": "flopscost-",
+               "qwen3-32b-shard-numel-maxflops": "numel-maxflops-"}[name]
+        w = shard_of(full, own, r, f"qwen3-32b-R32-{tag}shard{r}")
+        extras = {"R": full.R, "alpha": full.alpha, "cost": cost, "plan_rank": r,
+                  "planned_from": f"{QWEN32_LAYOUT}; Algorithm 1 with R = 32, alpha = 1, W(p) = {cost}; "
+                                  f"plan rank {r}" + (f", {what}" if rank == 0 else f", the {rank + 1}-th by load")}
+        return w, [len(w.shapes)], 1, 1.0, 0, extras
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -323,62 +422,193 @@ ORACLE_WHOLE_FLOPS = 3e12   # shards up to this much Newton-Schulz work are time
 
 
 def time_oracle_sample(shapes, grad_std, seed=0):
-    """Times the fp64 oracle over the shard: every tensor when its Newton-Schulz work is
-    at most ORACLE_WHOLE_FLOPS (the tiny workload and the Qwen3-1.7B layer), else one
-    tensor of each distinct shape, extrapolated by multiplicity.
+    """Times the fp64 oracle, as it stands, on the shard or on a bounded sample of it.
+
+    A shard with at most ORACLE_WHOLE_FLOPS of Newton-Schulz work (the tiny workload, the Qwen3-1.7B layer) is
+    timed whole, every tensor through `muon_step_tensor`.  A larger one is sampled per Newton-Schulz shape class
+    (m = min, n = max of rows/cols; a tall tensor costs the oracle what its transpose does): one tensor of the
+    class runs `muon_step_tensor` with one Newton-Schulz step (momentum, normalisation, one step, scale, apply,
+    bf16 copy) and then one more `newton_schulz` step on an m x n iterate, so that the tensor's time is the first
+    plus (K - 1) times the second, extrapolated by the class's multiplicity.
     Returns (ms_per_step, sample_desc, cores)."""
     import numpy as np
 
     from oracle import muon as OM
 
-    flops = sum(NS_STEPS * (4 * min(r, c) ** 2 * max(r, c) + 2 * min(r, c) ** 3) for r, c in shapes)
-    whole = flops <= ORACLE_WHOLE_FLOPS
-    distinct = {}
-    for s in shapes:
-        distinct[s] = distinct.get(s, 0) + 1
-    todo = [(s, 1) for s in shapes] if whole else list(distinct.items())
+    flops = sum(ns_flops([s]) for s in shapes)
     rng = np.random.default_rng(seed)
+    if flops <= ORACLE_WHOLE_FLOPS:
+        total_ms = 0.0
+        for r, c in shapes:
+            W = (0.02 * rng.standard_normal((r, c))).astype(np.float32)
+            g = (grad_std * rng.standard_normal((r, c))).astype(np.float32)
+            m = np.zeros((r, c), np.float32)
+            t0 = time.perf_counter()
+            OM.muon_step_tensor(W, g, m, LR, MU, NS_STEPS)
+            total_ms += (time.perf_counter() - t0) * 1e3
+        desc = f"oracle (fp64 NumPy) on every tensor of the shard ({len(shapes)} tensors), timed whole"
+        return total_ms, desc, os.cpu_count() or 1
+    classes = {}
+    for r, c in shapes:
+        key = (min(r, c), max(r, c))
+        first, mult = classes.get(key, ((r, c), 0))
+        classes[key] = (first, mult + 1)
     total_ms = 0.0
     parts = []
-    for (r, c), mult in todo:
+    for (mm, nn), ((r, c), mult) in classes.items():
         W = (0.02 * rng.standard_normal((r, c))).astype(np.float32)
         g = (grad_std * rng.standard_normal((r, c))).astype(np.float32)
         m = np.zeros((r, c), np.float32)
         t0 = time.perf_counter()
-        OM.muon_step_tensor(W, g, m, LR, MU, NS_STEPS)
-        dt = (time.perf_counter() - t0) * 1e3
-        total_ms += dt * mult
-        parts.append(f"{r}x{c}")
-    if whole:
-        desc = f"oracle (fp64 NumPy) on every tensor of the shard ({len(shapes)} tensors), timed whole"
-    else:
-        desc = (f"oracle (fp64 NumPy) on one tensor of each distinct shape ({', '.join(parts)}; "
-                f"{len(distinct)} of {len(shapes)} tensors), extrapolated by multiplicity")
+        OM.muon_step_tensor(W, g, m, LR, MU, 1)
+        t_one = time.perf_counter() - t0
+        X = rng.standard_normal((mm, nn)) / np.sqrt(mm * nn)
+        t0 = time.perf_counter()
+        OM.newton_schulz(X, 1)
+        t_ns = time.perf_counter() - t0
+        total_ms += mult * (t_one + (NS_STEPS - 1) * t_ns) * 1e3
+        parts.append(f"{mm}x{nn} x{mult}")
+    desc = (f"oracle (fp64 NumPy), extrapolated: per Newton-Schulz shape class ({', '.join(parts)}; "
+            f"{len(shapes)} tensors) one tensor through muon_step_tensor with 1 Newton-Schulz step plus "
+            f"{NS_STEPS - 1} x one timed newton_schulz step, times the class's multiplicity")
     return total_ms, desc, os.cpu_count() or 1
 
 
+def step_config(w, my_shapes, extras, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    cfg = {"workload": w.name, "matrices": len(my_shapes), "elements": sum(r * c for r, c in my_shapes),
+           "ns_steps": NS_STEPS, "R": extras.get("R", 1), "alpha": extras.get("alpha", 1.0),
+           "l2": "flushed between timed steps: 256 MiB write, then 256 MiB read of another buffer",
+           "grad": "bf16" if w.grad_bf16 else "fp32", "parallelism": f"dp{world}"}
+    for k in ("cost", "plan_rank", "planned_from"):
+        if k in extras:
+            cfg[k] = extras[k]
+    return cfg
+
+
 def run_reference(args):
+    """The reference arm: the oracle, as it stands, on this run's rank-0 shard, timed on the host cores."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    from zero_sharded_gb300 import workloads as wl  # noqa: F401  (shapes only)
-
-    w, buckets, R, alpha, _ = build_workload(args.workload, 1, 0)
+    w, buckets, R, alpha, my_rank, extras = build_workload(args.workload, world, 0, planner="oracle")
+    owner, _ = plan_owner_load(w.numels, buckets, R, alpha, planner="oracle")
+    my_shapes = [s for s, o in zip(w.shapes, owner) if o == my_rank]
     for _ in range(args.warmup):
-        time_oracle_sample(w.shapes, w.grad_std)
+        time_oracle_sample(my_shapes, w.grad_std)
     vals = []
     desc, cores = "", 1
     for _ in range(args.steps):
-        ms, desc, cores = time_oracle_sample(w.shapes, w.grad_std)
+        ms, desc, cores = time_oracle_sample(my_shapes, w.grad_std)
         vals.append(ms)
     v = statistics.mean(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "ms", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "matrices": len(w.shapes), "elements": w.total, "ns_steps": NS_STEPS},
+            "config": step_config(w, my_shapes, extras, world),
             "cpu_baseline": {"value": v, "unit": "ms", "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_cost_compare(args):
+    """Both cost models of Algorithm 1 on the Qwen3-32B layout (R = 32, alpha = 1), measured on the GPU: every
+    distinct shard (the multiset of its tensor shapes) of the numel plan and of the Newton-Schulz-flops plan is
+    stepped `--steps` times after `--warmup` (L2 flushed before each step, CUDA events on the stream), and each
+    plan's slowest rank is reported.  The step is communication-free, so that rank sets the distributed
+    optimizer step time of the plan.  One GPU; prints one JSON line."""
+    from collections import Counter
+
+    import torch
+
+    from zero_sharded_gb300 import build as zbuild
+    from zero_sharded_gb300 import cz
+    from zero_sharded_gb300 import workloads as wl
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    if not os.path.exists(zbuild.LIB):
+        zbuild.build()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+    flush_rd = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        torch.sum(flush_rd)
+
+    plans = {}
+    for cost in ("numel", "flops"):
+        full, own, load = qwen32_plan(cost)
+        ranks = []
+        for r in range(full.R):
+            shapes = [s for s, o in zip(full.shapes, own) if o == r]
+            ranks.append((r, tuple(sorted(Counter(shapes).items())), shapes))
+        plans[cost] = (load, ranks)
+    distinct = {}
+    for cost in plans:
+        for r, key, shapes in plans[cost][1]:
+            distinct.setdefault(key, shapes)
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    clocks.mark_begin()
+    comp_ms = {}
+    for key, shapes in distinct.items():
+        if not shapes:
+            comp_ms[key] = 0.0
+            continue
+        w = wl.Workload("shard", list(shapes), [f"t{i}" for i in range(len(shapes))], 0.02, 1e-3)
+        plan = cz.cz_plan_partition(w.numels, [len(shapes)], 1, 1.0)
+        P = wl.draw(w.shapes, w.param_std, 0, device=dev)
+        G = wl.draw(w.shapes, w.grad_std, 1, device=dev)
+        M = torch.zeros_like(P)
+        PB = P.to(torch.bfloat16)
+        ws_bytes = cz.cz_workspace_size(plan, 0, w.shapes)
+        WS = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        sargs = cz.StepArgs(w.offsets, w.shapes)
+        opts = cz.make_opts(param_bf16=PB, workspace=WS, workspace_bytes=ws_bytes)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                flush_l2()
+                if i >= args.warmup:
+                    ev[i - args.warmup][0].record(stream)
+                cz.cz_muon_step_ex(plan, 0, P, G, M, sargs, LR, MU, NS_STEPS, stream, opts)
+                if i >= args.warmup:
+                    ev[i - args.warmup][1].record(stream)
+        torch.cuda.synchronize()
+        st = cz.cz_device_status(stream, WS)
+        if st != cz.CZ_OK:
+            raise SystemExit(f"device status: {cz.cz_status_string(st)}")
+        comp_ms[key] = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        del P, G, M, PB, WS
+        torch.cuda.empty_cache()
+    clocks.mark_end()
+    clk = clocks.stop()
+
+    out = {}
+    for cost, (load, ranks) in plans.items():
+        ms = [comp_ms[key] for _, key, _ in ranks]
+        tf = [ns_flops(shapes) / 1e12 for _, _, shapes in ranks]
+        slow = max(range(len(ranks)), key=lambda r: (ms[r], -r))
+        heavy = max(range(len(ranks)), key=lambda r: (load[r], -r))
+        out[cost] = {"slowest_rank": slow, "slowest_ms": ms[slow], "slowest_ns_tflop": tf[slow],
+                     "slowest_shard": {f"{a}x{b}": n for (a, b), n in ranks[slow][1]},
+                     "heaviest_load_rank": heavy, "heaviest_load_ms": ms[heavy],
+                     "max_rank_ns_tflop": max(tf), "mean_rank_ms": statistics.mean(ms),
+                     "rank_ms": ms, "rank_ns_tflop": tf}
+    line = {"mode": "plan-cost-compare", "metric": "Muon step ms of each plan's slowest shard", "unit": "ms",
+            "higher_is_better": False, "layout": QWEN32_LAYOUT + "; Algorithm 1, R = 32, alpha = 1",
+            "steps": args.steps, "warmup": args.warmup, "distinct_shards_timed": len(distinct),
+            "numel": out["numel"], "flops": out["flops"],
+            "slowest_ms_flops_over_numel": out["flops"]["slowest_ms"] / out["numel"]["slowest_ms"],
+            "max_ns_tflop_flops_over_numel": out["flops"]["max_rank_ns_tflop"] / out["numel"]["max_rank_ns_tflop"],
+            "clocks": clk, "data": "synthetic", "dtype": "bf16"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -390,14 +620,17 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["cz", "reference"], default="cz")
-    ap.add_argument("--workload", default="qwen3-1.7b-layer",
-                    choices=["qwen3-1.7b-layer", "tiny", "qwen3-1.7b-28L", "qwen3-14b-microgroup", "qwen3-32b-shard"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOADS)
+    ap.add_argument("--compare-cost", action="store_true",
+                    help="time every distinct shard of the Qwen3-32B layout under the numel and the flops plans")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-torch-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.compare_cost:
+        return run_cost_compare(args)
 
     import torch
     import torch.distributed as dist
@@ -416,7 +649,7 @@ def main():
 
     if not os.path.exists(zbuild.LIB):
         zbuild.build()
-    w, buckets, R, alpha, my_rank = build_workload(args.workload, world, rank)
+    w, buckets, R, alpha, my_rank, extras = build_workload(args.workload, world, rank)
     plan = cz.cz_plan_partition(w.numels, buckets, R, alpha)
     owner = plan.owner()
     my_shapes = [s for s, o in zip(w.shapes, owner) if o == my_rank]
@@ -506,7 +739,7 @@ def main():
     F = ns_flops(my_shapes)
     F_exec = ns_flops_executed(my_shapes)
     ns_tflops = F / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0
-    peak_t = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    ns_exec_tflops = F_exec / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else 0.0
     el = sum(r * c for r, c in my_shapes)
     # algorithmic bytes of the momentum pass: read g and m, write m and one bf16 copy of u
     mom_bytes = el * (10 + (2 if w.grad_bf16 else 4))
@@ -574,32 +807,38 @@ def main():
         te = torch.tensor([e_ms], device=dev)
         if world > 1:
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": float(te.item()) / world, "unit": "ms",
+        e2e = {"value": float(te.item()), "unit": "ms",
                "h2d_bytes_per_step": int(sum(hi - lo for lo, hi in own_rng) * G.element_size()),
                "d2h_bytes_per_step": int(sum(hi - lo for lo, hi in own_rng) * PB.element_size()),
                "overlap": "two copy streams; step j+1's gradient copy and step j's read-back overlap compute",
                "timing": "steady-state pipeline: (end of the last timed read-back - start of the first timed "
                          "gradient copy) / steps, no drain between the warm-up and the timed steps"}
 
-    # roofline of the dominant kernel (largest share of the step's device time)
+    # roofline of the dominant kernel (largest share of the step's device time).  The tensor cores execute the
+    # symmetric products' upper-triangle tiles only (and K padded to 64), so the rate held against the peak is the
+    # executed one; the dense count of the three products (K * sum(4m^2n + 2m^3)) is reported beside it.  The peak
+    # is the measured cuBLAS bf16 rate for the clock state sampled in the timed region: the sustained rate when
+    # the power cap was active, the burst rate otherwise.
+    reasons = (clk or {}).get("reasons", [])
+    capped = "sw_power_cap" in reasons
+    peak_key = "bf16_tflops_sustained" if capped else "bf16_tflops"
+    peak_t = float(peaks.get(peak_key, FALLBACK_PEAKS[peak_key]))
+    peak_note = (f"{peak_key} of {peak_src} (" + ("sw_power_cap active in the timed region" if capped else
+                 "no clock-event reason active in the timed region") + ")")
     dom = max(prof, key=lambda k: prof[k][0])
     dom_ms, dom_n = prof[dom][0], prof[dom][1]
     avg_ms = dom_ms / max(dom_n, 1)
     traffic = ncu_traffic(w.name, dom) if world == 1 else None
     if dom.startswith("ns_"):
-        per_launch = ns_flops_by_kind(my_shapes)[dom] * args.steps / max(dom_n, 1)
-        ach = per_launch / (avg_ms * 1e-3) / 1e12
+        ex_per_launch = ns_flops_executed_by_kind(my_shapes)[dom] * args.steps / max(dom_n, 1)
+        alg_per_launch = ns_flops_by_kind(my_shapes)[dom] * args.steps / max(dom_n, 1)
+        ach = ex_per_launch / (avg_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": f"ns_gemm_kernel ({dom})", "achieved": ach, "peak": peak_t,
                 "unit": "TFLOP/s", "frac": ach / peak_t if peak_t else None, "traffic": traffic,
-                "algorithmic_per_launch": per_launch, "launch_ms": avg_ms,
-                "peak_source": f"bf16_tflops_sustained of {peak_src}"}
-        if dom == "ns_fused":
-            # the launch runs every product of a step; the tensor cores execute the symmetric products'
-            # upper-triangle tiles only, so the executed rate is the one to hold against the peak
-            f_ex = ns_flops_executed([sh for sh in my_shapes if not _is_small(*sh)])
-            ex = f_ex / (avg_ms * 1e-3) / 1e12
-            roof.update({"executed_per_launch": f_ex, "executed_achieved": ex,
-                         "executed_frac": ex / peak_t if peak_t else None})
+                "flops": "executed", "executed_per_launch": ex_per_launch, "launch_ms": avg_ms,
+                "launches_per_step": dom_n / args.steps, "peak_source": peak_note,
+                "algorithmic_per_launch": alg_per_launch,
+                "algorithmic_achieved": alg_per_launch / (avg_ms * 1e-3) / 1e12}
     else:
         per_launch = mom_bytes
         ach = per_launch / (avg_ms * 1e-3) / 1e9
@@ -690,18 +929,17 @@ def main():
             cms, desc, cores = time_oracle_sample(my_shapes, w.grad_std)
             cpu = {"value": cms, "unit": "ms", "cores": cores, "kind": "oracle", "sample": desc}
         line = {
-            "metric": METRIC, "value": max_ms / world, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC, "value": max_ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "matrices": len(my_shapes), "elements": el, "ns_steps": NS_STEPS,
-                       "R": R, "alpha": alpha, "l2": "flushed between timed steps: 256 MiB write, then 256 MiB read of another buffer",
-                       "grad": "bf16" if w.grad_bf16 else "fp32", "parallelism": f"dp{world}"},
+            "config": step_config(w, my_shapes, extras, world),
+            "value_definition": "the slowest rank's mean step time over the timed steps (each GPU steps one shard)",
+            "ms_per_shard_job": max_ms / world,
             "roofline": roof,
-            "ns_all_phases": {"achieved": ns_tflops, "unit": "TFLOP/s", "peak": peak_t,
-                              "frac": ns_tflops / peak_t if peak_t else None,
-                              "peak_source": f"bf16_tflops_sustained of {peak_src}",
-                              "flops_per_step": F, "executed_flops_per_step": F_exec,
-                              "executed_tflops": F_exec / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else None,
+            "ns_all_phases": {"executed_tflops": ns_exec_tflops, "unit": "TFLOP/s", "peak": peak_t,
+                              "executed_frac": ns_exec_tflops / peak_t if peak_t else None,
+                              "peak_source": peak_note, "executed_flops_per_step": F_exec,
+                              "algorithmic_flops_per_step": F, "algorithmic_tflops": ns_tflops,
                               "launches_per_step": ns_launch, "ms_per_step": ns_ms},
             "momentum_pass": {"bound": "hbm", "achieved": mom_gbs, "peak": hbm, "unit": "GB/s",
                               "frac": mom_gbs / hbm if hbm else None, "bytes_per_element": mom_bytes / max(el, 1),

@@ -38,7 +38,7 @@ def _worker(rank, world, port, out_dir):
     from zero_sharded_gb300 import cz
     from zero_sharded_gb300 import workloads as wl
 
-    w, buckets, R, alpha, my_rank = bench.build_workload("tiny", world, rank)
+    w, buckets, R, alpha, my_rank, _ = bench.build_workload("tiny", world, rank)
     assert R == world and my_rank == rank
     plan = cz.cz_plan_partition(w.numels, buckets, R, alpha)
     owner = torch.tensor(plan.owner(), dtype=torch.int32)
@@ -66,7 +66,7 @@ def test_two_ranks_over_gloo(tmp_path):
     from oracle import muon as OM
     from zero_sharded_gb300 import workloads as wl
 
-    w, buckets, R, alpha, _ = bench.build_workload("tiny", world, 0)
+    w, buckets, R, alpha, _, _ = bench.build_workload("tiny", world, 0)
     owner = np.load(tmp_path / "owner0.npy")
     assert set(owner.tolist()) == {0, 1}                  # both ranks own tensors
     p, g, m = wl.make_state(w, seed=0)
