@@ -777,24 +777,31 @@ def main():
         ev_step = [torch.cuda.Event() for _ in range(n)]
         ev_d2h = [torch.cuda.Event() for _ in range(n)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # diagnostics: each timed step's compute and each timed gradient copy, on their own streams
+        tse = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        tce = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
         torch.cuda.synchronize()
         for i in range(n):
             b = i & 1
-            if i == args.warmup:
-                # steady state: the pipeline keeps running from the warm-up steps into the timed ones
-                # (no drain), as in a training loop; the region opens where the first timed step's
-                # gradient copy starts and closes when the last timed step's read-back ends
-                t0.record(h2d)
             with torch.cuda.stream(h2d):
                 if i >= 2:
                     h2d.wait_event(ev_step[i - 2])             # the device buffer's previous user is done
+                if i == args.warmup:
+                    # steady state: the pipeline keeps running from the warm-up steps into the timed ones
+                    # (no drain), as in a training loop; the region opens where the first timed step's
+                    # gradient copy starts and closes when the last timed step's read-back ends
+                    t0.record(h2d)
+                tce[i][0].record(h2d)
                 for lo, hi in own_rng:
                     Gd[b][lo:hi].copy_(Gh[lo:hi], non_blocking=True)
+                tce[i][1].record(h2d)
                 ev_h2d[i].record(h2d)
             stream.wait_event(ev_h2d[i])
             if i >= 2:
                 stream.wait_event(ev_d2h[i - 2])             # bf16 buffer read back before it is rewritten
+            tse[i][0].record(stream)
             cz.cz_muon_step_ex(plan, my_rank, P, Gd[b], M, sargs, LR, MU, NS_STEPS, stream, optsd[b])
+            tse[i][1].record(stream)
             ev_step[i].record(stream)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(ev_step[i])
@@ -804,6 +811,9 @@ def main():
         t1.record(d2h)
         torch.cuda.synchronize()
         e_ms = t0.elapsed_time(t1) / args.steps
+        timed = range(args.warmup, n)
+        e2e_step_ms = statistics.mean(tse[i][0].elapsed_time(tse[i][1]) for i in timed)
+        e2e_h2d_ms = statistics.mean(tce[i][0].elapsed_time(tce[i][1]) for i in timed)
         te = torch.tensor([e_ms], device=dev)
         if world > 1:
             dist.all_reduce(te, op=dist.ReduceOp.MAX)
@@ -811,6 +821,7 @@ def main():
                "h2d_bytes_per_step": int(sum(hi - lo for lo, hi in own_rng) * G.element_size()),
                "d2h_bytes_per_step": int(sum(hi - lo for lo, hi in own_rng) * PB.element_size()),
                "overlap": "two copy streams; step j+1's gradient copy and step j's read-back overlap compute",
+               "step_ms_inside": e2e_step_ms, "h2d_ms_per_step": e2e_h2d_ms,
                "timing": "steady-state pipeline: (end of the last timed read-back - start of the first timed "
                          "gradient copy) / steps, no drain between the warm-up and the timed steps"}
 
