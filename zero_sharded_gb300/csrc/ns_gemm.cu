@@ -735,13 +735,18 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
   }
 }
 
-// CZ_NS_COOPERATIVE=0 launches the fused kernel without the cooperative attribute,
-// for tools that cannot replay a cooperative cluster launch; its units are then
-// co-resident only because the grid is the occupancy limit.
+// The fused launch is cooperative unless CZ_NS_COOPERATIVE=0 or a CUDA tool is
+// injected into the process (CUDA_INJECTION64_PATH set, as Nsight Compute,
+// Nsight Systems and compute-sanitizer do).  Nsight Compute's kernel profiling
+// fails a cooperative cluster launch with LaunchFailed and then shuts the
+// application down; such tools serialise launches, so the units of the fused
+// grid (the occupancy limit) are co-resident there without the attribute.
 bool cooperative_fused() {
   static const bool on = [] {
     const char* e = std::getenv("CZ_NS_COOPERATIVE");
-    return !(e && e[0] == '0');
+    if (e && e[0] == '0') return false;
+    const char* tool = std::getenv("CUDA_INJECTION64_PATH");
+    return !(tool && tool[0]);
   }();
   return on;
 }
