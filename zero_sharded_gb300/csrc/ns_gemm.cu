@@ -736,17 +736,22 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
 }
 
 // The fused launch is cooperative unless CZ_NS_COOPERATIVE=0 or a CUDA tool is
-// injected into the process (CUDA_INJECTION64_PATH set, as Nsight Compute,
-// Nsight Systems and compute-sanitizer do).  Nsight Compute's kernel profiling
-// fails a cooperative cluster launch with LaunchFailed and then shuts the
-// application down; such tools serialise launches, so the units of the fused
-// grid (the occupancy limit) are co-resident there without the attribute.
+// attached to the process: Nsight Compute (it sets NV_COMPUTE_PROFILER_PERFWORKS_DIR
+// and NV_NSIGHT_INJECTION_TRANSPORT_TYPE in the target) or a tool injected through
+// CUDA_INJECTION64_PATH.  Nsight Compute's kernel profiling fails a cooperative
+// cluster launch with LaunchFailed and then shuts the application down; such tools
+// serialise launches, so the units of the fused grid (the occupancy limit) are
+// co-resident there without the attribute.
 bool cooperative_fused() {
   static const bool on = [] {
     const char* e = std::getenv("CZ_NS_COOPERATIVE");
     if (e && e[0] == '0') return false;
-    const char* tool = std::getenv("CUDA_INJECTION64_PATH");
-    return !(tool && tool[0]);
+    for (const char* v : {"NV_COMPUTE_PROFILER_PERFWORKS_DIR", "NV_NSIGHT_INJECTION_TRANSPORT_TYPE",
+                          "CUDA_INJECTION64_PATH"}) {
+      const char* t = std::getenv(v);
+      if (t && t[0]) return false;
+    }
+    return true;
   }();
   return on;
 }
