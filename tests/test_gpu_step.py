@@ -270,6 +270,19 @@ def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
     assert torch.equal(on["P"], plain["P"])
 
 
+@pytest.mark.parametrize("ns_steps", [5, 2])
+def test_fused_schedule_and_list_walk_are_bit_identical(tmp_path, ns_steps):
+    """The fused launch walks the host's dependency-aware schedule (each unit's tiles of every step in
+    one sequence) or, with CZ_NS_SCHED=0, the per-(step, product) lists: the same tiles with the same
+    K order and epilogues in another order across units, so the same bits, and one launch per step."""
+    shapes = [(384, 1024), (1024, 384), (256, 256), (128, 640), (640, 640)]
+    on = _run_child(tmp_path, "CZ_NS_SCHED", "1", shapes, ns_steps=ns_steps)
+    off = _run_child(tmp_path, "CZ_NS_SCHED", "0", shapes, ns_steps=ns_steps)
+    assert on["launches"]["ns_fused"] == 2 and off["launches"]["ns_fused"] == 2
+    assert torch.equal(on["P"], off["P"])
+    assert torch.equal(on["M"], off["M"])
+
+
 _SCHED_CHILD = r"""
 import json, sys, numpy as np, torch
 from zero_sharded_gb300 import cz

@@ -21,6 +21,7 @@
 #include <map>
 #include <memory>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -34,6 +35,11 @@ namespace {
 constexpr int64_t kAlign = 256;
 constexpr int64_t kDefaultTimeoutNs = 1000000000LL;   // 1 s per device-side wait
 constexpr int64_t kMaxNsSteps = 64;
+// The fused launch's dependency-aware schedule covers up to this many Newton-Schulz
+// steps, for shards whose bf16 iterate is at most kSchedMaxXBytes (above any L2
+// size: the fused launch only runs shards whose iterate fits the L2).
+constexpr int64_t kSchedMaxSteps = 16;
+constexpr int64_t kSchedMaxXBytes = 256LL << 20;
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -71,6 +77,10 @@ struct Layout {
   int64_t n_cta_entries = 0;
   int64_t off_expect = 0;          // fused launch: n_mats x 3 expected arrivals (int32)
   int64_t off_done = 0;            // fused launch: 3 x kMaxNsSteps x n_mats counters (int32), zero in the tables
+  int64_t off_sched_first = 0;     // fused launch schedule: kMaxGrid + 1 offsets (int32)
+  int64_t off_sched = 0;           // and its entries (int4), room for kSchedMaxSteps steps
+  int64_t sched_per_step = 0;      // tiles of one Newton-Schulz step (Gram + Poly + Update)
+  int64_t sched_cap = 0;           // entries the schedule region holds (0: no schedule)
   int64_t bytes = 0;
 };
 
@@ -176,6 +186,24 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
   L.off_cta = off; off = align_up(off + 4 * L.n_cta_entries, kAlign);
   L.off_expect = off; off = align_up(off + 4 * 3 * std::max<int64_t>(n_mats, 1), kAlign);
   L.off_done = off; off = align_up(off + 4 * 3 * kMaxNsSteps * std::max<int64_t>(n_mats, 1), kAlign);
+  // the fused launch's schedule, for shards small enough to take it
+  {
+    int64_t per_step = 0, xb = 0;
+    for (const Group& G : L.groups) {
+      if (G.small) continue;
+      // counted with 128-row tiles, which cover the CTA-pair variant's 256-row tiles too
+      int64_t sym = 0;
+      for (int64_t a = 0; a < ceil_div64(G.m, kBM); ++a)
+        for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b)
+          if (a * kBM <= b * kBN + kBN - 1) ++sym;
+      per_step += G.count * (2 * sym + ceil_div64(G.m, kBM) * ceil_div64(G.n, kBN));
+      xb += 2 * (int64_t)G.m * G.n * G.count;
+    }
+    L.sched_per_step = per_step;
+    L.sched_cap = xb <= kSchedMaxXBytes ? kSchedMaxSteps * per_step : 0;
+  }
+  L.off_sched_first = off; off = align_up(off + 4 * (kMaxGrid + 1), kAlign);
+  L.off_sched = off; off = align_up(off + 16 * std::max<int64_t>(L.sched_cap, 1), kAlign);
   // per-tile partial sums of the momentum pass: written before they are read, so outside the tables
   // that are copied in on every call
   L.off_partial = off; off = align_up(off + 4 * std::max<int64_t>(L.n_mom_tiles, 1), kAlign);
@@ -212,6 +240,16 @@ bool use_fused() {
     return !(e && e[0] == '0');
   }();
   return fused;
+}
+
+// The fused launch walks the host's dependency-aware schedule (default);
+// CZ_NS_SCHED=0 walks the per-(step, product) tile lists instead.
+bool use_sched() {
+  static const bool on = [] {
+    const char* e = std::getenv("CZ_NS_SCHED");
+    return !(e && e[0] == '0');
+  }();
+  return on;
 }
 
 // L2 size of the current device, in bytes (0 if it cannot be read).
@@ -267,6 +305,7 @@ struct Program {
   uint64_t uid = next_uid();
   bool pair = true;
   bool fused_ok = false;
+  int32_t sched_steps = 0;      // the fused launch's schedule is for this many steps (0: none)
   GemmParams fused{};
   Layout L;
   std::vector<uint8_t> host_tables;   // image of the workspace's [tables_begin, tables_end)
@@ -489,6 +528,103 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
   return true;
 }
 
+// Dependency-aware order of the fused launch's tiles (list scheduling on a model of
+// the launch).  The launch runs, per matrix, a chain of stages (Gram, Poly, Update of
+// step 1, of step 2, ...); a tile may start once every tile of its matrix's previous
+// stage has finished and the hand-off (store completion, counter release, poll,
+// first operand load) is over.  Walking fixed per-(step, product) lists, a unit
+// stops at a tile whose matrix is not ready although later tiles of other matrices
+// are.  Here a model of the units (a tile takes its k-blocks plus a constant; a
+// hand-off takes kSchedHandoff k-blocks) assigns tiles as units free up, ready tiles
+// first, by the longest remaining chain of their matrix (critical path), then the
+// most k-blocks.  Each unit's sequence is in model time order, and every tile's
+// dependencies finish before it starts in the model, so the real launch cannot wait
+// in a cycle: the earliest blocked tile's dependencies are always running or queued
+// behind tiles that are not blocked.
+constexpr int64_t kSchedTileOverhead = 2;   // k-blocks: tile start and accumulator hand-off
+constexpr int64_t kSchedHandoff = 36;       // k-blocks: stage hand-off (about 12 us at 2 GHz)
+
+struct SchedItem { int4 e; int64_t kb; int32_t gm; };
+
+// lists: the seven fused lists' problems in GemmParams::lists order, prob_off their
+// problem offsets; per_unit receives each unit's entries.
+void schedule_fused(const std::vector<ProbDesc>* const lists[kFusedLists], const int32_t prob_off[kFusedLists],
+                    int steps, int units, int n_mats, std::vector<std::vector<int4>>& per_unit) {
+  // tiles of each (list, matrix), and the k-blocks of each (matrix, product)
+  std::vector<std::vector<std::vector<SchedItem>>> by(kFusedLists, std::vector<std::vector<SchedItem>>(n_mats));
+  std::vector<int64_t> maxkb((size_t)n_mats * 3, 0);
+  for (int li = 0; li < kFusedLists; ++li) {
+    const int slot = li < 2 ? 0 : li == 2 ? 1 : 2;
+    for (size_t i = 0; i < lists[li]->size(); ++i) {
+      const ProbDesc& pd = (*lists[li])[i];
+      const int64_t kb = ceil_div64(pd.gp.K, kBK);
+      for (const int4& t : pd.tiles) {
+        const int32_t gm = pd.gp.mat_base + t.y;
+        by[li][gm].push_back({make_int4(prob_off[li] + (int)i, t.y, t.z, t.w), kb, gm});
+        maxkb[(size_t)gm * 3 + slot] = std::max(maxkb[(size_t)gm * 3 + slot], kb);
+      }
+    }
+  }
+  auto list_of = [&](int t, int sl) { return sl == 0 ? (t & 1) : sl == 1 ? 2 : (t + 1 == steps ? 5 : 3) + (t & 1); };
+  const int64_t n_stages = (int64_t)steps * 3;
+  auto rem = [&](int32_t gm, int64_t stage) {   // model time from this stage's start to the chain's end
+    int64_t r = 0;
+    for (int64_t q = stage; q < n_stages; ++q) r += maxkb[(size_t)gm * 3 + q % 3] + kSchedTileOverhead + kSchedHandoff;
+    return r;
+  };
+  std::vector<int64_t> left((size_t)n_mats * n_stages, 0), last((size_t)n_mats * n_stages, 0);
+  for (int32_t gm = 0; gm < n_mats; ++gm)
+    for (int64_t q = 0; q < n_stages; ++q) left[(size_t)gm * n_stages + q] = (int64_t)by[list_of((int)(q / 3), (int)(q % 3))][gm].size();
+  // ready tiles: (priority, k-blocks, -matrix, -sequence) largest first
+  struct Ready { int64_t prio, kb; int32_t gm; int64_t seq; int64_t stage; int4 e; };
+  auto rless = [](const Ready& a, const Ready& b) {
+    if (a.prio != b.prio) return a.prio < b.prio;
+    if (a.kb != b.kb) return a.kb < b.kb;
+    if (a.gm != b.gm) return a.gm > b.gm;
+    return a.seq > b.seq;
+  };
+  std::priority_queue<Ready, std::vector<Ready>, decltype(rless)> ready(rless);
+  using Rel = std::tuple<int64_t, int32_t, int64_t>;   // (time, matrix, stage)
+  std::priority_queue<Rel, std::vector<Rel>, std::greater<Rel>> release;
+  using Unit = std::pair<int64_t, int>;                // (free time, unit)
+  std::priority_queue<Unit, std::vector<Unit>, std::greater<Unit>> free_units;
+  for (int32_t gm = 0; gm < n_mats; ++gm)
+    if (left[(size_t)gm * n_stages] > 0) release.emplace(0, gm, 0);
+  for (int u = 0; u < units; ++u) free_units.emplace(0, u);
+  per_unit.assign((size_t)units, {});
+  int64_t seq = 0, todo = 0;
+  for (int64_t x : left) todo += x;
+  while (todo > 0) {
+    auto [tf, u] = free_units.top();
+    free_units.pop();
+    while (!release.empty() && std::get<0>(release.top()) <= tf) {
+      auto [rt, gm, q] = release.top();
+      release.pop();
+      const int t = (int)(q / 3);
+      const int64_t pr = rem(gm, q);
+      for (const SchedItem& it : by[list_of(t, (int)(q % 3))][gm]) {
+        int4 e = it.e;
+        e.x |= t << 8;
+        ready.push({pr, it.kb, gm, seq++, q, e});
+      }
+    }
+    if (ready.empty()) {        // nothing can start before the next stage is released
+      free_units.emplace(std::get<0>(release.top()), u);
+      continue;
+    }
+    const Ready r = ready.top();
+    ready.pop();
+    per_unit[(size_t)u].push_back(r.e);
+    const int64_t end = tf + r.kb + kSchedTileOverhead;
+    const size_t k = (size_t)r.gm * n_stages + r.stage;
+    last[k] = std::max(last[k], end);
+    if (--left[k] == 0 && r.stage + 1 < n_stages)   // the matrix's next stage (every stage has tiles)
+      release.emplace(last[k] + kSchedHandoff, r.gm, r.stage + 1);
+    --todo;
+    free_units.emplace(end, u);
+  }
+}
+
 int build_program(const Plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
                   const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps,
                   const cz_step_opts& o, uint8_t* ws, Program& P) {
@@ -703,7 +839,6 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     ml(kUpdate, upd[cur], P.update[cur], cur, fused_candidate ? &cu : nullptr);
     ml(kApply, app[cur], P.apply[cur], cur, fused_candidate ? &ca : nullptr);
   }
-  (void)ns_steps;
   SmallParams& sp = P.small;
   sp.mats = reinterpret_cast<const SmallMat*>(ws + L.off_small);
   sp.n_mats = n_small;
@@ -772,6 +907,36 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     F.expect = reinterpret_cast<const int*>(ws + L.off_expect);
     F.done = reinterpret_cast<int*>(ws + L.off_done);
     P.fused_ok = true;
+    // the dependency-aware schedule for the step count of this first call (other
+    // step counts walk the per-(step, product) lists)
+    if (use_sched() && ns_steps >= 1 && ns_steps <= kSchedMaxSteps && F.grid <= kMaxGrid) {
+      const std::vector<ProbDesc>* const pl[kFusedLists] = {&gram[0], &gram[1], &poly,  &upd[0],
+                                                             &upd[1],  &app[0],  &app[1]};
+      int32_t poff[kFusedLists];
+      for (int li = 0; li < kFusedLists; ++li) poff[li] = F.lists[li].prob_off;
+      std::vector<std::vector<int4>> per_unit;
+      schedule_fused(pl, poff, ns_steps, F.grid, (int)n_mats, per_unit);
+      int64_t entries = 0;
+      for (const auto& v : per_unit) entries += (int64_t)v.size();
+      if (entries <= L.sched_cap) {
+        const int64_t end = align_up(L.off_sched + 16 * entries, 16);
+        if (end > P.tables_end) {
+          P.tables_end = end;
+          img.resize((size_t)(P.tables_end - tb), 0);
+        }
+        int32_t* sf = at<int32_t>(img, tb, L.off_sched_first);
+        int4* se = at<int4>(img, tb, L.off_sched);
+        int32_t pos = 0;
+        for (int u = 0; u < F.grid; ++u) {
+          sf[u] = pos;
+          for (const int4& e : per_unit[(size_t)u]) se[pos++] = e;
+        }
+        sf[F.grid] = pos;
+        F.sched = reinterpret_cast<const int4*>(ws + L.off_sched);
+        F.sched_first = reinterpret_cast<const int32_t*>(ws + L.off_sched_first);
+        P.sched_steps = ns_steps;
+      }
+    }
   }
   // The small-matrix CTAs beside the tiled products' units: only when all of them
   // fit on the GPU at once (then neither waits for the other's SMs).
@@ -1021,6 +1186,10 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   if (P.fused_ok && use_fused() && ns_steps <= kMaxNsSteps) {
     gp = P.fused;
     gp.ns_steps = ns_steps;
+    if (ns_steps != P.sched_steps) {   // the schedule is for another step count
+      gp.sched = nullptr;
+      gp.sched_first = nullptr;
+    }
     scalars(gp);
     const cudaError_t e = traced(6, s, [&] { return launch_ns_gemm(kFused, P.pair, gp, s); });
     if (e == cudaSuccess) return CZ_OK;

@@ -288,9 +288,10 @@ __device__ __forceinline__ void apply_chunk(const GemmParams& p, const GemmProbl
 }
 
 // The tiles a unit (CTA or CTA pair) processes, in order.  A per-phase launch
-// walks its own range of p.tiles.  The fused launch walks, for every Newton-Schulz
-// step, the unit's ranges of the Gram, Poly and Update (Apply in the last step)
-// lists, so all three roles see the same sequence without a fused tile list.
+// walks its own range of p.tiles.  The fused launch walks the unit's sequence of
+// the host's schedule (p.sched) when there is one; otherwise, for every
+// Newton-Schulz step, the unit's ranges of the Gram, Poly and Update (Apply in the
+// last step) lists.  All three roles see the same sequence either way.
 template <int PHASE>
 struct Walker {
   const GemmParams& p;
@@ -316,6 +317,20 @@ struct Walker {
       sl = 0;
       return true;
     } else {
+      if (p.sched) {
+        // the host's dependency-aware schedule: this unit's tiles of every step, in order
+        if (!open) {
+          j = p.sched_first[unit];
+          j_end = p.sched_first[unit + 1];
+          open = true;
+        }
+        if (j >= j_end) return false;
+        tl = p.sched[j++];
+        prob = tl.x & 0xFF;
+        iter = tl.x >> 8;
+        sl = p.prob[prob].slot;
+        return true;
+      }
       while (true) {
         const TileList& L = p.lists[list_of(it, slot)];
         if (!open) {

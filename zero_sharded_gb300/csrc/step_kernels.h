@@ -147,6 +147,11 @@ struct GemmParams {
   TileList lists[kFusedLists];
   int* done;              // (3 * ns_steps) x n_mats completion counters, zero at launch
   const int* expect;      // n_mats x 3: arrivals that complete (matrix, slot)
+  // or null: every unit's tiles of all steps in one scheduled sequence, in place of
+  // the per-(step, product) lists: entry {problem | step << 8, matrix, tile_m, tile_n},
+  // unit b runs entries [sched_first[b], sched_first[b+1])
+  const int4* sched;
+  const int32_t* sched_first;
 };
 
 // Dynamic shared memory of the GEMM kernel.
