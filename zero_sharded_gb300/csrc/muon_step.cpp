@@ -442,22 +442,27 @@ struct ProbDesc {
 // contiguously, heaviest first; cta_first gives the ranges.
 struct TileRef { int4 t; int64_t cost; };
 
-// Tiles of one matrix in an L2-friendly order.  Consecutive list entries run at
-// the same time (one per unit), so the list walks the larger operand in groups of
-// `group` row blocks while sweeping the smaller operand fully inside each group:
-// the group's large blocks plus the whole small operand stay in L2, and each large
-// block is read from HBM once instead of once per row of tiles.
-// big_is_n: the B side (tile_n index) is the large operand.
-void grouped_tiles(std::vector<int4>& out, int mat, int64_t TM, int64_t TN, bool big_is_n, int64_t group) {
-  if (group < 1) group = 1;
-  if (big_is_n) {
+// Tiles of one matrix's Update (B' X, B' m x m, X m x n) in an L2-friendly order.
+// Consecutive entries run at the same time, one per unit, so a wave of `units`
+// entries reads the B' row blocks and the X column blocks of its tiles.  Each X
+// column block is read by one wave only, while B' is read again by every wave, so
+// B' must stay in the L2 from wave to wave.  At m = 5120 (B' 52 MB) it did not: the
+// Update read 4.5x its algorithmic bytes from DRAM.  B' rows are therefore split
+// into parts of at most kUpdateBBytes each; a wave covers one part's row blocks and
+// as many X column blocks as fill the units, and X is swept once per part.  Two
+// parts at m = 5120: DRAM reads -22% and the Qwen3-32B shard's step 55.18 ->
+// 54.41 ms (the step runs at the power cap, where less DRAM traffic means clock);
+// three parts read X once more than they save.
+constexpr int64_t kUpdateBBytes = 32LL << 20;
+
+void update_tiles(std::vector<int4>& out, int mat, int64_t m, int64_t TM, int64_t TN, int64_t units) {
+  const int64_t parts = std::min<int64_t>(TM, std::max<int64_t>(1, ceil_div64(2 * m * m, kUpdateBBytes)));
+  for (int64_t sp = 0; sp < parts; ++sp) {
+    const int64_t a_lo = sp * TM / parts, a_hi = (sp + 1) * TM / parts;
+    const int64_t group = std::max<int64_t>(1, ceil_div64(units, a_hi - a_lo));
     for (int64_t b0 = 0; b0 < TN; b0 += group)
-      for (int64_t a = 0; a < TM; ++a)
+      for (int64_t a = a_lo; a < a_hi; ++a)
         for (int64_t b = b0; b < std::min(TN, b0 + group); ++b) out.push_back(make_int4(0, mat, (int)a, (int)b));
-  } else {
-    for (int64_t a0 = 0; a0 < TM; a0 += group)
-      for (int64_t b = 0; b < TN; ++b)
-        for (int64_t a = a0; a < std::min(TM, a0 + group); ++a) out.push_back(make_int4(0, mat, (int)a, (int)b));
   }
 }
 
@@ -788,8 +793,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       d.tot = d.to;
       // update tiles: B' (m x m) is the small operand, X (m x n) the large one
       const int64_t TMu = ceil_div64(G.m, tm_rows), TNu = ceil_div64(G.n, kBN);
-      const int64_t grp_u = ceil_div64(max_grid, TMu);
-      for (int j = 0; j < c; ++j) grouped_tiles(d.tiles, j, TMu, TNu, true, grp_u);
+      for (int j = 0; j < c; ++j) update_tiles(d.tiles, j, G.m, TMu, TNu, max_grid);
       upd[cur].push_back(d);
       // apply: the same product, the epilogue writes W (X for a wide tensor, X^T for a tall one)
       ProbDesc e = d;
