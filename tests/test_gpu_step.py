@@ -283,6 +283,47 @@ def test_fused_schedule_and_list_walk_are_bit_identical(tmp_path, ns_steps):
     assert torch.equal(on["M"], off["M"])
 
 
+_STEPS_CHILD = r"""
+import json, sys, numpy as np, torch
+from zero_sharded_gb300 import cz
+from zero_sharded_gb300 import workloads as wl
+shapes = [tuple(x) for x in json.loads(sys.argv[2])]
+counts = json.loads(sys.argv[3])
+numels = [r * c for r, c in shapes]
+offsets = list(np.cumsum([0] + numels[:-1]))
+plan = cz.cz_plan_partition(numels, [len(shapes)], 1, 1.0)
+P = wl.draw(shapes, 0.02, 41).cuda()
+M = torch.zeros_like(P)
+for k, n in enumerate(counts):
+    G = wl.draw(shapes, 1.0, 42 + k).cuda()
+    cz.cz_muon_step(plan, 0, P, G, M, cz.StepArgs(offsets, shapes), 0.02, 0.95, n)
+torch.cuda.synchronize()
+assert cz.cz_device_status(None, None) == cz.CZ_OK
+torch.save({"P": P.cpu(), "M": M.cpu()}, sys.argv[1])
+"""
+
+
+def test_schedule_built_for_the_first_step_count_only(tmp_path):
+    """The fused launch's schedule is built for the step count of the first call on a set of buffers;
+    later calls with another count walk the lists.  Five calls of 5, 3, 5, 17 and 2 steps on the same
+    buffers give the same bits with the schedule as with the lists alone (CZ_NS_SCHED=0)."""
+    import json
+    import os
+    import subprocess
+    import sys
+    shapes = [(384, 1024), (1024, 384), (256, 256), (640, 640)]
+    counts = [5, 3, 5, 17, 2]
+    out = {}
+    for sched in ("1", "0"):
+        f = tmp_path / f"steps_{sched}.pt"
+        r = subprocess.run([sys.executable, "-c", _STEPS_CHILD, str(f), json.dumps(shapes), json.dumps(counts)],
+                           env=dict(os.environ, CZ_NS_SCHED=sched), capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        out[sched] = torch.load(f)
+    assert torch.equal(out["1"]["P"], out["0"]["P"])
+    assert torch.equal(out["1"]["M"], out["0"]["M"])
+
+
 _SCHED_CHILD = r"""
 import json, sys, numpy as np, torch
 from zero_sharded_gb300 import cz
