@@ -5,10 +5,14 @@
 // [s_{i,r-1}, s_{i,r}) of every bucket, with no communication, because each
 // owned tensor is whole on the rank.  This file selects the owned tensors from
 // the plan, groups them by Newton-Schulz shape (m = min, n = max of rows/cols),
-// lays out the device workspace, builds TMA tensor maps and LPT-ordered tile
-// lists once per (plan, rank, buffers) and then enqueues, on the caller's stream:
-//   momentum pass -> per-tensor norm -> ns_steps x (Gram, Poly, Update) where
-//   the last Update is the fused apply.
+// lays out the device workspace, and builds once per (plan, rank, buffers) a step
+// program: TMA tensor maps, LPT-assigned tile lists in L2-friendly order, and,
+// for shards whose iterate fits the L2, the fused launch's dependency-aware
+// schedule.  Every call then enqueues, on the caller's stream: the copy of the
+// program's tables into the workspace -> the momentum pass (with the per-tensor
+// norm) -> either one fused launch for every Newton-Schulz product of every step,
+// or ns_steps x (Gram, Poly, Update) launches, the last Update fused with the
+// apply; small matrices run all their steps on chip, beside the tiled ones.
 
 #include <cuda.h>
 #include <cuda_runtime.h>

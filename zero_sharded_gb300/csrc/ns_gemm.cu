@@ -1,9 +1,9 @@
 // Newton-Schulz GEMMs on the 5th-generation tensor cores (sm_103a).
 //
-// One kernel template, one launch per Newton-Schulz product, grouped over every
-// owned tensor of the shard (tensors of the same shape form one batched
-// "problem"; a launch carries up to kMaxProblems of them and a flat tile list).
-// All products are D = A * B^T with bf16 operands and an fp32 accumulator in TMEM:
+// One kernel template over the product it runs and over the tile geometry.  All
+// products are D = A * B^T with bf16 operands and an fp32 accumulator in TMEM,
+// grouped over every owned tensor of the shard (tensors of one shape form a
+// batched "problem"; a launch carries up to kMaxProblems of them):
 //   Gram    A  = X X^T                  operands X rows, X rows      (K = n, both K-major)
 //   Poly    B' = a I + b A + c A A^T    operands A rows, A rows      (K = m), A symmetric
 //   Update  X' <- B' X                  operands B' rows (K-major), X (MN-major: K = m
@@ -11,27 +11,34 @@
 // a X + B X = (a I + B) X, so the a X term rides in the Poly output and the
 // Update epilogue reads no operand.  X is kept only in its m x n orientation, in
 // two buffers: the Update reads one and writes the other (tiles of one column
-// block read every row of X).  Step 1 folds the Frobenius
-// normalisation in as scalars: A_1 = s^2 X~X~^T and X_1 = s B'_1 X~,
-// s = 1/(||u||_F + eps).  The last Update instead runs the apply epilogue:
-// W <- W - lr*sqrt(max(1,rows/cols)) * X_K in fp32, the bf16 parameter copy,
-// and (optionally) the applied delta.
+// block read every row of X).  Step 1 folds the Frobenius normalisation in as
+// scalars: A_1 = s^2 X~X~^T and X_1 = s B'_1 X~, s = 1/(||u||_F + eps).  The last
+// Update instead runs the apply epilogue: W <- W - lr*sqrt(max(1,rows/cols)) * X_K
+// in fp32, the bf16 parameter copy, and (optionally) the applied delta.
 //
-// Structure (one CTA per SM, persistent over a static round-robin tile list):
-//   warp 0      TMA producer: 128x64 (A side) and 256x64 (B side) bf16 tiles,
-//               128-byte swizzle, kStages-deep mbarrier ring
-//   warp 1      TMEM allocation (512 columns = two 128x256 fp32 accumulators)
-//               and the single thread that issues tcgen05.mma (M=128, N=256, K=16)
-//   warps 2..9  epilogue, two warps per TMEM lane quarter (each takes half of the
-//               tile's 256 columns): tcgen05.ld 32 columns at a time, phase math,
-//               then the 32 x 32 block is staged in smem (as is and transposed)
-//               and written with TMA bulk tensor stores, which clip at the
-//               tensor's edges.  The global operands an epilogue chunk needs
-//               (A for Poly, W for the apply) are loaded one chunk ahead, the
-//               first chunk's before waiting for the accumulator.
-// The TMEM double buffer lets the epilogue of tile i overlap the mainloop of i+1.
-// For the symmetric products only tiles touching the upper triangle are
-// computed.
+// Launches: one per product (PHASE = kGram .. kApply), each unit walking its
+// range of an LPT-assigned tile list; or one for every product of every step
+// (kFused), each unit walking the host's dependency-aware schedule (or the
+// per-(step, product) lists), with per-(matrix, step, product) completion
+// counters ordering the stages of each matrix.
+//
+// Structure of a unit: by default a CTA pair (cluster of 2, tcgen05 cta_group::2)
+// computes a 256 x 256 tile; CZ_NS_PAIR=0 gives one CTA per 128 x 256 tile.  Per CTA:
+//   warp 0      TMA producer (one lane): its 128 rows of the A side and its share of
+//               the B side per 64-wide k-block, 128-byte swizzle, an mbarrier ring
+//   warp 1      TMEM allocation (512 columns: two 256-column fp32 accumulators) and,
+//               in the even CTA, the one lane that issues tcgen05.mma (M = 256 across
+//               the pair, N = 256, K = 16) and its commits
+//   warps 2..   epilogue, one or two warps per TMEM lane quarter: tcgen05.ld 32
+//               columns at a time, the phase's math, then each 32 x 32 block is
+//               staged in smem (as is and, above the diagonal of a symmetric
+//               product, transposed) and written with TMA bulk tensor stores,
+//               which clip at the tensor's edges; the apply updates W directly.
+//               The global operands an epilogue chunk needs (A for Poly, W for
+//               the apply) are loaded one chunk ahead.
+// The TMEM double buffer lets the epilogue of tile i overlap the main loop of
+// i + 1.  For the symmetric products only tiles touching the upper triangle are
+// computed.  Every wait is bounded (see ptx.cuh).
 
 #include <cuda_bf16.h>
 
