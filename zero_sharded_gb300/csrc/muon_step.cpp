@@ -458,6 +458,7 @@ struct TileRef { int4 t; int64_t cost; };
 // 54.41 ms (the step runs at the power cap, where less DRAM traffic means clock);
 // three parts read X once more than they save.
 constexpr int64_t kUpdateBBytes = 32LL << 20;
+constexpr int64_t kSymBlock = 8;   // tiles per side of a block of the symmetric products' tile order
 
 void update_tiles(std::vector<int4>& out, int mat, int64_t m, int64_t TM, int64_t TN, int64_t units) {
   const int64_t parts = std::min<int64_t>(TM, std::max<int64_t>(1, ceil_div64(2 * m * m, kUpdateBBytes)));
@@ -751,12 +752,21 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     uint16_t* B = reinterpret_cast<uint16_t*>(ws + G.off_b);
     const int64_t msx = (int64_t)G.m * G.ldx, msa = (int64_t)G.m * G.ldm;
     const int c = G.count;
-    // symmetric tiles of an m x m output
+    // symmetric tiles of an m x m output: the tiles touching the upper triangle, in
+    // blocks of kSymBlock x kSymBlock tiles, so that a wave of consecutive tiles reads
+    // fewer row blocks of its operand (Qwen3-32B shard: 54.12 -> 53.90 ms per step,
+    // Gram DRAM reads -1.5%, Poly -15%; row by row, column by column and diagonal
+    // bands read as much or more)
     std::vector<int4> sym;
-    for (int j = 0; j < c; ++j)
-      for (int64_t a = 0; a < ceil_div64(G.m, tm_rows); ++a)
-        for (int64_t b = 0; b < ceil_div64(G.m, kBN); ++b)
-          if (a * tm_rows <= b * kBN + kBN - 1) sym.push_back(make_int4(0, j, (int)a, (int)b));
+    {
+      const int64_t TA = ceil_div64(G.m, tm_rows), TB = ceil_div64(G.m, kBN);
+      for (int j = 0; j < c; ++j)
+        for (int64_t i0 = 0; i0 < TA; i0 += kSymBlock)
+          for (int64_t j0 = 0; j0 < TB; j0 += kSymBlock)
+            for (int64_t a = i0; a < std::min(TA, i0 + kSymBlock); ++a)
+              for (int64_t b = j0; b < std::min(TB, j0 + kSymBlock); ++b)
+                if (a * tm_rows <= b * kBN + kBN - 1) sym.push_back(make_int4(0, j, (int)a, (int)b));
+    }
     for (int cur = 0; cur < 2; ++cur) {
       // Gram: A = s^2 X X^T from X buffer `cur`, stored with its mirror into A
       ProbDesc d{};
