@@ -557,8 +557,10 @@ constexpr int64_t kSchedHandoff = 36;       // k-blocks: stage hand-off (about 1
 struct SchedItem { int4 e; int64_t kb; int32_t gm; };
 
 // lists: the seven fused lists' problems in GemmParams::lists order, prob_off their
-// problem offsets; per_unit receives each unit's entries.
-void schedule_fused(const std::vector<ProbDesc>* const lists[kFusedLists], const int32_t prob_off[kFusedLists],
+// problem offsets; per_unit receives each unit's entries.  Returns false (and the
+// caller walks the lists) if the model ever had no tile to start and no stage to
+// wait for, which the stage chains rule out.
+bool schedule_fused(const std::vector<ProbDesc>* const lists[kFusedLists], const int32_t prob_off[kFusedLists],
                     int steps, int units, int n_mats, std::vector<std::vector<int4>>& per_unit) {
   // tiles of each (list, matrix), and the k-blocks of each (matrix, product)
   std::vector<std::vector<std::vector<SchedItem>>> by(kFusedLists, std::vector<std::vector<SchedItem>>(n_mats));
@@ -619,6 +621,7 @@ void schedule_fused(const std::vector<ProbDesc>* const lists[kFusedLists], const
       }
     }
     if (ready.empty()) {        // nothing can start before the next stage is released
+      if (release.empty()) return false;
       free_units.emplace(std::get<0>(release.top()), u);
       continue;
     }
@@ -633,6 +636,7 @@ void schedule_fused(const std::vector<ProbDesc>* const lists[kFusedLists], const
     --todo;
     free_units.emplace(end, u);
   }
+  return true;
 }
 
 int build_program(const Plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
@@ -933,10 +937,10 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       int32_t poff[kFusedLists];
       for (int li = 0; li < kFusedLists; ++li) poff[li] = F.lists[li].prob_off;
       std::vector<std::vector<int4>> per_unit;
-      schedule_fused(pl, poff, ns_steps, F.grid, (int)n_mats, per_unit);
+      const bool scheduled = schedule_fused(pl, poff, ns_steps, F.grid, (int)n_mats, per_unit);
       int64_t entries = 0;
       for (const auto& v : per_unit) entries += (int64_t)v.size();
-      if (entries <= L.sched_cap) {
+      if (scheduled && entries <= L.sched_cap) {
         const int64_t end = align_up(L.off_sched + 16 * entries, 16);
         if (end > P.tables_end) {
           P.tables_end = end;
