@@ -271,6 +271,19 @@ def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
 
 
 @pytest.mark.parametrize("ns_steps", [5, 2])
+def test_latency_bound_fused_launch_is_bit_identical(tmp_path, ns_steps):
+    """A shard whose products all have fewer tiles than the GPU has units runs the fused launch with
+    twice the epilogue warps (its stage chains are the whole launch); the same tiles and epilogue math
+    as one launch per product, so the same bits."""
+    shapes = [(256, 256), (256, 512), (384, 640), (512, 256)]
+    on = _run_child(tmp_path, "CZ_NS_FUSED", "1", shapes, ns_steps=ns_steps)
+    off = _run_child(tmp_path, "CZ_NS_FUSED", "0", shapes, ns_steps=ns_steps)
+    assert on["launches"]["ns_fused"] == 2 and off["launches"]["ns_fused"] == 0
+    assert torch.equal(on["P"], off["P"])
+    assert torch.equal(on["M"], off["M"])
+
+
+@pytest.mark.parametrize("ns_steps", [5, 2])
 def test_fused_schedule_and_list_walk_are_bit_identical(tmp_path, ns_steps):
     """The fused launch walks the host's dependency-aware schedule (each unit's tiles of every step in
     one sequence) or, with CZ_NS_SCHED=0, the per-(step, product) lists: the same tiles with the same

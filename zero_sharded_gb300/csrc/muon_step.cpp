@@ -309,6 +309,7 @@ struct Program {
   uint64_t uid = next_uid();
   bool pair = true;
   bool fused_ok = false;
+  int32_t fused_phase = kFused;  // kFusedLatency when every product has fewer tiles than units
   int32_t sched_steps = 0;      // the fused launch's schedule is for this many steps (0: none)
   GemmParams fused{};
   Layout L;
@@ -879,8 +880,11 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   // cannot happen: both regions are sized by build_layout
   if (cursor > L.n_gemm_tiles || cta_cursor > L.n_cta_entries) return CZ_ERR_NOMEM;
 
+  // the fused launch's variant: a shard whose products all have fewer tiles than the
+  // units waits on every stage's epilogue, so it runs twice the epilogue warps
+  P.fused_phase = most < max_grid ? kFusedLatency : kFused;
   // expected arrivals per (matrix, slot): tiles of the matrix x epilogue warps per unit
-  const int arrivals = kFusedEpiWarps * (pair ? 2 : 1);
+  const int arrivals = epi_warps(P.fused_phase) * (pair ? 2 : 1);
   int32_t* expect = at<int32_t>(img, tb, L.off_expect);
   for (auto& pd : gram[0])
     for (const int4& t : pd.tiles) expect[(pd.gp.mat_base + t.y) * 3 + 0] += arrivals;
@@ -1213,7 +1217,7 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
       gp.sched_first = nullptr;
     }
     scalars(gp);
-    const cudaError_t e = traced(6, s, [&] { return launch_ns_gemm(kFused, P.pair, gp, s); });
+    const cudaError_t e = traced(6, s, [&] { return launch_ns_gemm(P.fused_phase, P.pair, gp, s); });
     if (e == cudaSuccess) return CZ_OK;
     // The runtime refused the launch (e.g. it cannot guarantee that all units are
     // resident at once): clear the error and run one launch per product instead.

@@ -311,7 +311,7 @@ struct Walker {
   }
   // Next tile: its entry, global problem index, Newton-Schulz step and slot.
   __device__ bool next(int4& tl, int& prob, int& iter, int& sl) {
-    if constexpr (PHASE != kFused) {
+    if constexpr (!is_fused(PHASE)) {
       if (!open) {
         j = p.cta_first[unit];
         j_end = p.cta_first[unit + 1];
@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
       int prob, iter, sl;
       while (ok && walk.next(tl, prob, iter, sl)) {
         const GemmProblem& pr = p.prob[prob];
-        if constexpr (PHASE == kFused) {
+        if constexpr (is_fused(PHASE)) {
           // the matrix's previous stage must be complete (and visible) before its data is loaded
           const int* ctr;
           int target;
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
     while (walk.next(tl, prob, iter, sl)) {
       const GemmProblem& pr = p.prob[prob];
       bool ok;
-      if constexpr (PHASE == kFused) {
+      if constexpr (is_fused(PHASE)) {
         const bool first = iter == 0;
         switch (pr.phase) {
           case kGram: ok = epilogue_tile<kGram, PAIR, EW>(p, e, pr, prob, tl.y, tl.z, tl.w, first, acc, acc_phase); break;
@@ -807,7 +807,7 @@ cudaError_t launch_phase(const GemmParams& p, cudaStream_t s) {
     attr[n_attr].val.clusterDim.z = 1;
     ++n_attr;
   }
-  if constexpr (PHASE == kFused) {
+  if constexpr (is_fused(PHASE)) {
     if (cooperative_fused()) {
       attr[n_attr].id = cudaLaunchAttributeCooperative;
       attr[n_attr].val.cooperative = 1;
@@ -834,6 +834,8 @@ cudaError_t launch_ns_gemm(int phase, bool pair, const GemmParams& p, cudaStream
     case kApply * 2 + 1: return launch_phase<kApply, true>(p, s);
     case kFused * 2: return launch_phase<kFused, false>(p, s);
     case kFused * 2 + 1: return launch_phase<kFused, true>(p, s);
+    case kFusedLatency * 2: return launch_phase<kFusedLatency, false>(p, s);
+    case kFusedLatency * 2 + 1: return launch_phase<kFusedLatency, true>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }

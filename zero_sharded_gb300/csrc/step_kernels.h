@@ -74,7 +74,9 @@ enum Phase : int32_t {
   kUpdate = 2,   // X' <- s B' X into the other X buffer (= s (a X + B X))
   kApply = 3,    // last step: W <- W - lr*scale*s B' X, transposed for a tall W (+ bf16 copy, debug delta)
   kFused = 4,    // every product of all ns_steps in one launch, per-matrix dependencies
+  kFusedLatency = 5,   // the same with twice the epilogue warps (shards with fewer tiles per product than units)
 };
+__host__ __device__ constexpr bool is_fused(int phase) { return phase == kFused || phase == kFusedLatency; }
 
 // One batched GEMM: `count` matrices of the same M x N x K, operands read by
 // the two tensor maps of the same index (A side: M rows, B side: N rows), output
@@ -158,7 +160,12 @@ struct GemmParams {
 // Epilogue warps: two per TMEM lane quarter for the one-product launches (the apply's
 // master-weight traffic wants the memory parallelism), one per quarter for the fused
 // launch (fewer warps competing with the producer and MMA threads for issue slots;
-// measured faster there, slower for the per-product Poly and Apply).
+// measured faster there, slower for the per-product Poly and Apply).  A shard whose
+// products all have fewer tiles than there are units waits on each stage's epilogue
+// (its matrices' stage chains are the whole launch): there the fused launch runs two
+// epilogue warps per quarter as well (kFusedLatency; six small matrices and one
+// 256 x 256 one: 0.157 -> 0.142 ms per step; on the Qwen3-1.7B layer, 8 warps were
+// 2.7% slower than 4).
 constexpr int kEpiWarps = 8;                                  // the most any variant uses (shared memory)
 constexpr int kFusedEpiWarps = 4;
 __host__ __device__ constexpr int epi_warps(int phase) { return phase == kFused ? kFusedEpiWarps : kEpiWarps; }
