@@ -129,12 +129,12 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("78f0bc763c325705", {"qwen3-1.7b-layer": {"ns_fused": 2610.79e6},
+    "ns_gemm": ("26909f0df7fee12a", {"qwen3-1.7b-layer": {"ns_fused": 2610.79e6},
                                      "qwen3-32b-R32-shard4": {"ns_gram": 13181.62e6, "ns_poly": 948.67e6,
                                                               "ns_update": 16741.82e6, "ns_update_apply": 28450.74e6}}),
-    "momentum": ("45e49a36449b9ed1", {"qwen3-1.7b-layer": {"momentum": 645.92e6},
+    "momentum": ("2df37d1f608c2ab2", {"qwen3-1.7b-layer": {"momentum": 645.92e6},
                                       "qwen3-32b-R32-shard4": {"momentum": 14626.35e6}}),
-    "ns_small": ("d043421a3d7df772", {"tiny": {"ns_small": 0.3438e6}}),
+    "ns_small": ("7528803a819f4d42", {"tiny": {"ns_small": 0.3438e6}}),
     "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 
