@@ -118,7 +118,7 @@ def ns_flops_executed_by_kind(shapes, steps=NS_STEPS, bn=256):
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures summarised
 # under profiles/, per kernel kind, keyed by a hash of the sources that kernel is built and launched from:
 # once one of them changes the figure no longer describes the kernel and the bench reports null.
-STEP_SOURCES = ["muon_step.cpp", "ptx.cuh", "step_kernels.h", "cz_internal.h"]
+STEP_SOURCES = ["muon_step.cpp", "fused_schedule.h", "ptx.cuh", "step_kernels.h", "cz_internal.h"]
 KERNEL_SOURCES = {
     "ns_gemm": ["ns_gemm.cu"] + STEP_SOURCES,
     "momentum": ["momentum.cu"] + STEP_SOURCES,
@@ -129,12 +129,12 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("26909f0df7fee12a", {"qwen3-1.7b-layer": {"ns_fused": 2610.79e6},
+    "ns_gemm": ("6a3fa8453d316cb5", {"qwen3-1.7b-layer": {"ns_fused": 2610.79e6},
                                      "qwen3-32b-R32-shard4": {"ns_gram": 13181.62e6, "ns_poly": 948.67e6,
                                                               "ns_update": 16741.82e6, "ns_update_apply": 28450.74e6}}),
-    "momentum": ("2df37d1f608c2ab2", {"qwen3-1.7b-layer": {"momentum": 645.92e6},
+    "momentum": ("ddd7e264084bbb3c", {"qwen3-1.7b-layer": {"momentum": 645.92e6},
                                       "qwen3-32b-R32-shard4": {"momentum": 14626.35e6}}),
-    "ns_small": ("7528803a819f4d42", {"tiny": {"ns_small": 0.3438e6}}),
+    "ns_small": ("667c52192a390437", {"tiny": {"ns_small": 0.3438e6}}),
     "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 

@@ -31,6 +31,7 @@
 #include <vector>
 
 #include "cz_internal.h"
+#include "fused_schedule.h"
 #include "step_kernels.h"
 
 namespace cz {
@@ -539,107 +540,6 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
   return true;
 }
 
-// Dependency-aware order of the fused launch's tiles (list scheduling on a model of
-// the launch).  The launch runs, per matrix, a chain of stages (Gram, Poly, Update of
-// step 1, of step 2, ...); a tile may start once every tile of its matrix's previous
-// stage has finished and the hand-off (store completion, counter release, poll,
-// first operand load) is over.  Walking fixed per-(step, product) lists, a unit
-// stops at a tile whose matrix is not ready although later tiles of other matrices
-// are.  Here a model of the units (a tile takes its k-blocks plus a constant; a
-// hand-off takes kSchedHandoff k-blocks) assigns tiles as units free up, ready tiles
-// first, by the longest remaining chain of their matrix (critical path), then the
-// most k-blocks.  Each unit's sequence is in model time order, and every tile's
-// dependencies finish before it starts in the model, so the real launch cannot wait
-// in a cycle: the earliest blocked tile's dependencies are always running or queued
-// behind tiles that are not blocked.
-constexpr int64_t kSchedTileOverhead = 2;   // k-blocks: tile start and accumulator hand-off
-constexpr int64_t kSchedHandoff = 36;       // k-blocks: stage hand-off (about 12 us at 2 GHz)
-
-struct SchedItem { int4 e; int64_t kb; int32_t gm; };
-
-// lists: the seven fused lists' problems in GemmParams::lists order, prob_off their
-// problem offsets; per_unit receives each unit's entries.  Returns false (and the
-// caller walks the lists) if the model ever had no tile to start and no stage to
-// wait for, which the stage chains rule out.
-bool schedule_fused(const std::vector<ProbDesc>* const lists[kFusedLists], const int32_t prob_off[kFusedLists],
-                    int steps, int units, int n_mats, std::vector<std::vector<int4>>& per_unit) {
-  // tiles of each (list, matrix), and the k-blocks of each (matrix, product)
-  std::vector<std::vector<std::vector<SchedItem>>> by(kFusedLists, std::vector<std::vector<SchedItem>>(n_mats));
-  std::vector<int64_t> maxkb((size_t)n_mats * 3, 0);
-  for (int li = 0; li < kFusedLists; ++li) {
-    const int slot = li < 2 ? 0 : li == 2 ? 1 : 2;
-    for (size_t i = 0; i < lists[li]->size(); ++i) {
-      const ProbDesc& pd = (*lists[li])[i];
-      const int64_t kb = ceil_div64(pd.gp.K, kBK);
-      for (const int4& t : pd.tiles) {
-        const int32_t gm = pd.gp.mat_base + t.y;
-        by[li][gm].push_back({make_int4(prob_off[li] + (int)i, t.y, t.z, t.w), kb, gm});
-        maxkb[(size_t)gm * 3 + slot] = std::max(maxkb[(size_t)gm * 3 + slot], kb);
-      }
-    }
-  }
-  auto list_of = [&](int t, int sl) { return sl == 0 ? (t & 1) : sl == 1 ? 2 : (t + 1 == steps ? 5 : 3) + (t & 1); };
-  const int64_t n_stages = (int64_t)steps * 3;
-  auto rem = [&](int32_t gm, int64_t stage) {   // model time from this stage's start to the chain's end
-    int64_t r = 0;
-    for (int64_t q = stage; q < n_stages; ++q) r += maxkb[(size_t)gm * 3 + q % 3] + kSchedTileOverhead + kSchedHandoff;
-    return r;
-  };
-  std::vector<int64_t> left((size_t)n_mats * n_stages, 0), last((size_t)n_mats * n_stages, 0);
-  for (int32_t gm = 0; gm < n_mats; ++gm)
-    for (int64_t q = 0; q < n_stages; ++q) left[(size_t)gm * n_stages + q] = (int64_t)by[list_of((int)(q / 3), (int)(q % 3))][gm].size();
-  // ready tiles: (priority, k-blocks, -matrix, -sequence) largest first
-  struct Ready { int64_t prio, kb; int32_t gm; int64_t seq; int64_t stage; int4 e; };
-  auto rless = [](const Ready& a, const Ready& b) {
-    if (a.prio != b.prio) return a.prio < b.prio;
-    if (a.kb != b.kb) return a.kb < b.kb;
-    if (a.gm != b.gm) return a.gm > b.gm;
-    return a.seq > b.seq;
-  };
-  std::priority_queue<Ready, std::vector<Ready>, decltype(rless)> ready(rless);
-  using Rel = std::tuple<int64_t, int32_t, int64_t>;   // (time, matrix, stage)
-  std::priority_queue<Rel, std::vector<Rel>, std::greater<Rel>> release;
-  using Unit = std::pair<int64_t, int>;                // (free time, unit)
-  std::priority_queue<Unit, std::vector<Unit>, std::greater<Unit>> free_units;
-  for (int32_t gm = 0; gm < n_mats; ++gm)
-    if (left[(size_t)gm * n_stages] > 0) release.emplace(0, gm, 0);
-  for (int u = 0; u < units; ++u) free_units.emplace(0, u);
-  per_unit.assign((size_t)units, {});
-  int64_t seq = 0, todo = 0;
-  for (int64_t x : left) todo += x;
-  while (todo > 0) {
-    auto [tf, u] = free_units.top();
-    free_units.pop();
-    while (!release.empty() && std::get<0>(release.top()) <= tf) {
-      auto [rt, gm, q] = release.top();
-      release.pop();
-      const int t = (int)(q / 3);
-      const int64_t pr = rem(gm, q);
-      for (const SchedItem& it : by[list_of(t, (int)(q % 3))][gm]) {
-        int4 e = it.e;
-        e.x |= t << 8;
-        ready.push({pr, it.kb, gm, seq++, q, e});
-      }
-    }
-    if (ready.empty()) {        // nothing can start before the next stage is released
-      if (release.empty()) return false;
-      free_units.emplace(std::get<0>(release.top()), u);
-      continue;
-    }
-    const Ready r = ready.top();
-    ready.pop();
-    per_unit[(size_t)u].push_back(r.e);
-    const int64_t end = tf + r.kb + kSchedTileOverhead;
-    const size_t k = (size_t)r.gm * n_stages + r.stage;
-    last[k] = std::max(last[k], end);
-    if (--left[k] == 0 && r.stage + 1 < n_stages)   // the matrix's next stage (every stage has tiles)
-      release.emplace(last[k] + kSchedHandoff, r.gm, r.stage + 1);
-    --todo;
-    free_units.emplace(end, u);
-  }
-  return true;
-}
-
 int build_program(const Plan* plan, int32_t rank, float* flat_param, const void* flat_grad, float* flat_mom,
                   const int64_t* offsets, const int64_t* shapes, float lr, float mu, int32_t ns_steps,
                   const cz_step_opts& o, uint8_t* ws, Program& P) {
@@ -936,12 +836,19 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
     // the dependency-aware schedule for the step count of this first call (other
     // step counts walk the per-(step, product) lists)
     if (use_sched() && ns_steps >= 1 && ns_steps <= kSchedMaxSteps && F.grid <= kMaxGrid) {
+      static_assert(kSchedLists == kFusedLists, "the schedule walks the fused lists");
       const std::vector<ProbDesc>* const pl[kFusedLists] = {&gram[0], &gram[1], &poly,  &upd[0],
                                                              &upd[1],  &app[0],  &app[1]};
-      int32_t poff[kFusedLists];
-      for (int li = 0; li < kFusedLists; ++li) poff[li] = F.lists[li].prob_off;
-      std::vector<std::vector<int4>> per_unit;
-      const bool scheduled = schedule_fused(pl, poff, ns_steps, F.grid, (int)n_mats, per_unit);
+      std::vector<SchedTile> st[kFusedLists];
+      for (int li = 0; li < kFusedLists; ++li)
+        for (size_t i = 0; i < pl[li]->size(); ++i) {
+          const ProbDesc& pd = (*pl[li])[i];
+          for (const int4& t : pd.tiles)
+            st[li].push_back({F.lists[li].prob_off + (int32_t)i, t.y, t.z, t.w, pd.gp.mat_base + t.y,
+                              ceil_div64(pd.gp.K, kBK)});
+        }
+      std::vector<std::vector<SchedEntry>> per_unit;
+      const bool scheduled = schedule_fused(st, ns_steps, F.grid, (int)n_mats, per_unit);
       int64_t entries = 0;
       for (const auto& v : per_unit) entries += (int64_t)v.size();
       if (scheduled && entries <= L.sched_cap) {
@@ -955,7 +862,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         int32_t pos = 0;
         for (int u = 0; u < F.grid; ++u) {
           sf[u] = pos;
-          for (const int4& e : per_unit[(size_t)u]) se[pos++] = e;
+          for (const SchedEntry& e : per_unit[(size_t)u]) se[pos++] = make_int4(e.x, e.y, e.z, e.w);
         }
         sf[F.grid] = pos;
         F.sched = reinterpret_cast<const int4*>(ws + L.off_sched);
