@@ -239,13 +239,13 @@ torch.save({"P": P.cpu(), "M": M.cpu(), "launches": {k: v[1] for k, v in prof.it
 """
 
 
-def _run_child(tmp_path, env_name, env_value, shapes, ns_steps=5):
+def _run_child(tmp_path, env_name, env_value, shapes, ns_steps=5, extra_env=None):
     import json
     import os
     import subprocess
     import sys
     f = tmp_path / f"out_{env_name}_{env_value}.pt"
-    e = dict(os.environ, **{env_name: env_value})
+    e = dict(os.environ, **{env_name: env_value}, **(extra_env or {}))
     r = subprocess.run([sys.executable, "-c", _CHILD, str(f), json.dumps(shapes), str(ns_steps)], env=e,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
@@ -268,6 +268,19 @@ def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
     plain = _run_child(tmp_path, "CZ_NS_COOPERATIVE", "0", shapes)
     assert plain["launches"]["ns_fused"] == 2
     assert torch.equal(on["P"], plain["P"])
+
+
+@pytest.mark.parametrize("ns_steps", [5, 2])
+def test_paced_per_product_launches_are_bit_identical(tmp_path, ns_steps):
+    """One launch per product, each wave of tiles started together (a launch whose tiles all cost the
+    same) or not (CZ_NS_PACE=0): the same tiles on the same units in the same order, so the same bits.
+    The shapes mix K values, so some launches are paced and some are not."""
+    shapes = [(384, 1024), (1024, 384), (256, 256), (128, 640), (640, 640), (768, 768)]
+    paced = _run_child(tmp_path, "CZ_NS_PACE", "1", shapes, ns_steps=ns_steps, extra_env={"CZ_NS_FUSED": "0"})
+    plain = _run_child(tmp_path, "CZ_NS_PACE", "0", shapes, ns_steps=ns_steps, extra_env={"CZ_NS_FUSED": "0"})
+    assert paced["launches"]["ns_fused"] == 0 and paced["launches"]["ns_gram"] == 2 * ns_steps
+    assert torch.equal(paced["P"], plain["P"])
+    assert torch.equal(paced["M"], plain["M"])
 
 
 @pytest.mark.parametrize("ns_steps", [5, 2])

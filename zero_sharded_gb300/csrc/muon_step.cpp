@@ -247,6 +247,22 @@ bool use_fused() {
   return fused;
 }
 
+// One-product launches of equal-cost tiles start each wave of tiles together
+// (default): tiles that share an operand then read it at the same k, while it is
+// in the L2.  On the Qwen3-32B shard Gram's DRAM reads fell 27% per matrix and its
+// time 1.5-1.7%; the step went from 53.40 to 52.98 ms on one box and did not move
+// on another.  Without it the units drift apart over a launch of ~210 tiles each,
+// and a launch over 8 matrices read per matrix about twice what one over 2 read.
+// Letting units run up to 1, 2 or 4 waves apart did not help.  CZ_NS_PACE=0 turns
+// it off.
+bool use_pace() {
+  static const bool on = [] {
+    const char* e = std::getenv("CZ_NS_PACE");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
 // The fused launch walks the host's dependency-aware schedule (default);
 // CZ_NS_SCHED=0 walks the per-(step, product) tile lists instead.
 bool use_sched() {
@@ -300,6 +316,7 @@ struct Launch {
   int phase;
   int first;
   int cur;                          // X buffer read (Gram, Update, Apply)
+  bool uniform = false;             // every tile has the same k-blocks (wave pacing applies)
   GemmParams params;
 };
 
@@ -512,6 +529,8 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
     ln.phase = phase;
     ln.first = first;
     ln.cur = cur;
+    ln.uniform = true;
+    for (size_t i = c0 + 1; i < c1; ++i) ln.uniform = ln.uniform && probs[i].gp.K == probs[c0].gp.K;
     std::memset(&ln.params, 0, sizeof(GemmParams));
     ln.params = common;
     ln.params.n_prob = (int)(c1 - c0);
@@ -1116,6 +1135,10 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
   auto scalars = [&](GemmParams& g) {
     g.a = opts->a; g.b = opts->b; g.c = opts->c; g.lr = lr; g.lr_dev = opts->lr_device;
   };
+  auto refused = [](cudaError_t e) {
+    return e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorLaunchOutOfResources ||
+           e == cudaErrorNotSupported || e == cudaErrorInvalidConfiguration;
+  };
   if (P.fused_ok && use_fused() && ns_steps <= kMaxNsSteps) {
     gp = P.fused;
     gp.ns_steps = ns_steps;
@@ -1133,29 +1156,39 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
       return CZ_ERR_CUDA;
     cudaGetLastError();
   }
+  // One launch of a product.  A launch whose tiles all cost the same (round-robin
+  // lists: the units' list lengths differ by at most one) is paced by a counter of
+  // its own, one per (step, product) in the fused launch's completion counters
+  // (zeroed by every call's table copy; the fused launch does not run in a call
+  // that takes this path).  The least advanced unit never waits, so the pacing
+  // cannot deadlock once every unit is resident, which the cooperative attribute
+  // guarantees; a refused cooperative launch runs again unpaced.
+  int* pace_base = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + P.L.off_done);
+  const size_t pace_stride = (size_t)std::max<size_t>(P.L.mats.size(), 1);
+  auto run = [&](const Launch& ln, int phase, int kind, int first, int t, int slot) -> cudaError_t {
+    gp = ln.params;
+    gp.first = first;
+    scalars(gp);
+    gp.pace = (use_pace() && ln.uniform) ? pace_base + (size_t)(t * 3 + slot) * pace_stride : nullptr;
+    cudaError_t e = traced(kind, s, [&] { return launch_ns_gemm(phase, P.pair, gp, s); });
+    if (e != cudaSuccess && gp.pace && refused(e)) {
+      cudaGetLastError();
+      gp.pace = nullptr;
+      e = traced(kind, s, [&] { return launch_ns_gemm(phase, P.pair, gp, s); });
+    }
+    return e;
+  };
   for (int t = 0; t < ns_steps; ++t) {
     const int first = t == 0 ? 1 : 0;
     const int cur = t & 1;
-    for (const Launch& ln : P.gram[cur]) {
-      gp = ln.params;
-      gp.first = first;
-      scalars(gp);
-      if (traced(2, s, [&] { return launch_ns_gemm(kGram, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
-    }
-    for (const Launch& ln : P.poly) {
-      gp = ln.params;
-      scalars(gp);
-      if (traced(3, s, [&] { return launch_ns_gemm(kPoly, P.pair, gp, s); }) != cudaSuccess) return CZ_ERR_CUDA;
-    }
+    for (const Launch& ln : P.gram[cur])
+      if (run(ln, kGram, 2, first, t, 0) != cudaSuccess) return CZ_ERR_CUDA;
+    for (const Launch& ln : P.poly)
+      if (run(ln, kPoly, 3, 0, t, 1) != cudaSuccess) return CZ_ERR_CUDA;
     const bool final_step = t + 1 == ns_steps;
     const std::vector<Launch>& last = final_step ? P.apply[cur] : P.update[cur];
-    for (const Launch& ln : last) {
-      gp = ln.params;
-      gp.first = first;
-      scalars(gp);
-      if (traced(final_step ? 5 : 4, s, [&] { return launch_ns_gemm(ln.phase, P.pair, gp, s); }) != cudaSuccess)
-        return CZ_ERR_CUDA;
-    }
+    for (const Launch& ln : last)
+      if (run(ln, ln.phase, final_step ? 5 : 4, first, t, 2) != cudaSuccess) return CZ_ERR_CUDA;
   }
   return CZ_OK;
 }

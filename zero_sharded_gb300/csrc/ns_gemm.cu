@@ -562,8 +562,16 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
       Walker<PHASE> walk(p, unit);
       int4 tl;
       int prob, iter, sl;
+      int issued_tiles = 0;   // tiles whose loads this unit has issued (wave pacing)
       while (ok && walk.next(tl, prob, iter, sl)) {
         const GemmProblem& pr = p.prob[prob];
+        if constexpr (!is_fused(PHASE)) {
+          // wave pacing: this tile starts once every unit has issued as many tiles as this
+          // one (the even CTA paces; the odd one follows through the shared stage ring)
+          if (p.pace && rank == 0 && issued_tiles > 0 &&
+              !counter_wait(p.pace, issued_tiles * p.grid, abort, p.status, p.timeout_ns))
+            break;
+        }
         if constexpr (is_fused(PHASE)) {
           // the matrix's previous stage must be complete (and visible) before its data is loaded
           const int* ctr;
@@ -614,6 +622,10 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
             phase ^= 1u;
           }
         }
+        if constexpr (!is_fused(PHASE)) {
+          if (ok && p.pace && rank == 0) atomicAdd(p.pace, 1);
+        }
+        ++issued_tiles;
       }
       // every issued copy must land before the CTA may exit; a pair's copies are
       // counted on the even CTA's barriers, and the odd CTA waits for the even one
@@ -807,7 +819,9 @@ cudaError_t launch_phase(const GemmParams& p, cudaStream_t s) {
     attr[n_attr].val.clusterDim.z = 1;
     ++n_attr;
   }
-  if constexpr (is_fused(PHASE)) {
+  // The fused launch's units wait on one another's completion counters and paced
+  // units on one another's progress, so those launches are cooperative.
+  if (is_fused(PHASE) || p.pace) {
     if (cooperative_fused()) {
       attr[n_attr].id = cudaLaunchAttributeCooperative;
       attr[n_attr].val.cooperative = 1;
