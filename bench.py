@@ -129,12 +129,12 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("6a3fa8453d316cb5", {"qwen3-1.7b-layer": {"ns_fused": 2610.79e6},
-                                     "qwen3-32b-R32-shard4": {"ns_gram": 13181.62e6, "ns_poly": 948.67e6,
-                                                              "ns_update": 16741.82e6, "ns_update_apply": 28450.74e6}}),
-    "momentum": ("ddd7e264084bbb3c", {"qwen3-1.7b-layer": {"momentum": 645.92e6},
-                                      "qwen3-32b-R32-shard4": {"momentum": 14626.35e6}}),
-    "ns_small": ("667c52192a390437", {"tiny": {"ns_small": 0.3438e6}}),
+    "ns_gemm": ("4c9574d0407fd14e", {"qwen3-1.7b-layer": {"ns_fused": 2609.44e6},
+                                     "qwen3-32b-R32-shard4": {"ns_gram": 5905.42e6, "ns_poly": 993.29e6,
+                                                              "ns_update": 11092.40e6, "ns_update_apply": 24281.85e6}}),
+    "momentum": ("8dceb319f940472f", {"qwen3-1.7b-layer": {"momentum": 646.04e6},
+                                      "qwen3-32b-R32-shard4": {"momentum": 14626.36e6}}),
+    "ns_small": ("4aea293280e38ec6", {"tiny": {"ns_small": 0.3487e6}}),
     "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 
