@@ -52,11 +52,12 @@ def ns_flops(shapes, steps=NS_STEPS):
     return tot
 
 
-SMALL_M, SMALL_N = 128, 256     # matrices whose Newton-Schulz steps run on chip (ns_small)
+SMALL_M, SMALL_N = 128, 256     # matrices whose Newton-Schulz steps run on chip in one CTA (ns_small)
+SMALL_PAIR_M = 256              # ... and on a CTA pair, m up to this (the ns_small kind too)
 
 
 def _is_small(r, c):
-    return min(r, c) <= SMALL_M and max(r, c) <= SMALL_N
+    return min(r, c) <= SMALL_PAIR_M and max(r, c) <= SMALL_N
 
 
 def ns_flops_by_kind(shapes, steps=NS_STEPS):
@@ -74,7 +75,7 @@ def ns_flops_by_kind(shapes, steps=NS_STEPS):
 def ns_flops_executed(shapes, steps=NS_STEPS, bn=256):
     """Flops the tensor cores execute: 256x256 tiles on CTA pairs (128x256 with CZ_NS_PAIR=0), symmetric
     products on the tiles touching the upper triangle only; on-chip small matrices as 128-row products
-    with n padded to 64."""
+    with n padded to 64 (one CTA, m <= 128) or as 256 x 256 x 256 products (a CTA pair)."""
     bm = 128 if os.environ.get("CZ_NS_PAIR", "1") == "0" else 256
 
     def cdiv(a, b):
@@ -82,9 +83,12 @@ def ns_flops_executed(shapes, steps=NS_STEPS, bn=256):
     tot = 0
     for r, c in shapes:
         m, n = min(r, c), max(r, c)
-        if _is_small(r, c):
+        if _is_small(r, c) and m <= SMALL_M:
             n_pad = cdiv(n, 64) * 64
             tot += steps * (2 * 128 * 128 * n_pad + 2 * 128 * 128 * 128 + 2 * 128 * n_pad * 128)
+            continue
+        if _is_small(r, c):
+            tot += steps * 3 * 2 * SMALL_PAIR_M ** 3
             continue
         sym = sum(1 for a in range(cdiv(m, bm)) for b in range(cdiv(m, bn)) if a * bm <= b * bn + bn - 1)
         kpad_n, kpad_m = cdiv(n, 64) * 64, cdiv(m, 64) * 64
@@ -122,7 +126,7 @@ STEP_SOURCES = ["muon_step.cpp", "fused_schedule.h", "ptx.cuh", "step_kernels.h"
 KERNEL_SOURCES = {
     "ns_gemm": ["ns_gemm.cu"] + STEP_SOURCES,
     "momentum": ["momentum.cu"] + STEP_SOURCES,
-    "ns_small": ["ns_small.cu"] + STEP_SOURCES,
+    "ns_small": ["ns_small.cu", "ns_small_pair.cu"] + STEP_SOURCES,
     "apply": ["apply.cu"],
 }
 KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm", "ns_update": "ns_gemm",
@@ -753,8 +757,10 @@ def main():
     # Every step copies its fp32 (or bf16) gradients from pinned host memory and reads its bf16 parameters
     # back; the copies run on two copy streams and overlap the neighbouring steps' compute (device gradient
     # and bf16-parameter buffers are double-buffered; momentum and the fp32 master are shared, so steps stay
-    # ordered). Inputs (201 MB of gradients, 201 MB master, 201 MB momentum on the default layer) exceed the
-    # L2, so no flush is inserted. Value = (end of the last read-back - start of the first copy) / K.
+    # ordered). Inputs (4.19 GB of gradients, 4.19 GB master, 4.19 GB momentum on the Qwen3-32B shard) exceed
+    # the L2, so no flush is inserted. The warm-up steps are drained before the timed ones, so the window holds
+    # exactly the K timed steps: value = (end of the last read-back - start of the first gradient copy) / K,
+    # with the first copy and the last read-back exposed (nothing of the warm-up left to overlap them).
     e2e = None
     if not args.no_e2e:
         Gh = G.to("cpu").pin_memory()
@@ -789,9 +795,10 @@ def main():
                 if i >= 2:
                     h2d.wait_event(ev_step[i - 2])             # the device buffer's previous user is done
                 if i == args.warmup:
-                    # steady state: the pipeline keeps running from the warm-up steps into the timed ones
-                    # (no drain), as in a training loop; the region opens where the first timed step's
+                    # the warm-up steps are drained first (a copy that overlapped a warm-up step would put
+                    # that step's compute inside the window); the region opens where the first timed step's
                     # gradient copy starts and closes when the last timed step's read-back ends
+                    torch.cuda.synchronize()
                     t0.record(h2d)
                 tce[i][0].record(h2d)
                 for lo, hi in own_rng:
@@ -824,8 +831,8 @@ def main():
                "d2h_bytes_per_step": int(sum(hi - lo for lo, hi in own_rng) * PB.element_size()),
                "overlap": "two copy streams; step j+1's gradient copy and step j's read-back overlap compute",
                "step_ms_inside": e2e_step_ms, "h2d_ms_per_step": e2e_h2d_ms,
-               "timing": "steady-state pipeline: (end of the last timed read-back - start of the first timed "
-                         "gradient copy) / steps, no drain between the warm-up and the timed steps"}
+               "timing": "(end of the last timed read-back - start of the first timed gradient copy) / steps; "
+                         "warm-up drained before the first timed copy, copies of later steps overlap compute"}
 
     # roofline of the dominant kernel (largest share of the step's device time).  The tensor cores execute the
     # symmetric products' upper-triangle tiles only (and K padded to 64), so the rate held against the peak is the

@@ -226,10 +226,11 @@ int cz_workspace_size(const cz_plan* plan, int32_t rank, const int64_t* shapes, 
  * keeps the captured program's page-locked tables until the process exits.
  * Kernel timing (cz_profile_enable) skips captured launches.
  * Streams: all work is ordered on `stream`; when a shard has both small
- * matrices (m <= 128, n <= 256) and tiled ones, the small ones' launch may run
- * on a library-owned side stream (one per caller stream, never destroyed) that
- * is forked from `stream` after the momentum pass and joined back into it, so
- * that work enqueued on `stream` after the call still follows all of the step. */
+ * matrices (m <= 256, n <= 256) and tiled ones, or small matrices of both
+ * on-chip kinds (m <= 128 and 128 < m <= 256), one of the launches may run on a
+ * library-owned side stream (one per caller stream, never destroyed) that is
+ * forked from `stream` after the momentum pass and joined back into it, so that
+ * work enqueued on `stream` after the call still follows all of the step. */
 int cz_muon_step(const cz_plan* plan, int32_t rank,
                  float* flat_param, const void* flat_grad, float* flat_mom,
                  const int64_t* offsets, const int64_t* shapes,
@@ -298,7 +299,8 @@ int cz_device_status(void* stream, void* workspace, int* status_out);
  * step's launch tables into the workspace, 2 Gram (A = X X^T),
  * 3 Poly (B = bA + cA^2), 4 Update (X <- aX + BX), 5 Update fused with the apply,
  * 6 all Newton-Schulz products of a step in one launch (the default),
- * 7 every Newton-Schulz step of the small matrices (m <= 128, n <= 256) on chip.
+ * 7 every Newton-Schulz step of the small matrices (m <= 256, n <= 256) on chip
+ *   (one CTA per matrix for m <= 128, a CTA pair above).
  * ms and launches must hold n_kinds entries (n_kinds <= CZ_KERNEL_KINDS). */
 #define CZ_KERNEL_KINDS 8
 int cz_profile_enable(int32_t on);

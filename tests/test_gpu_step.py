@@ -489,9 +489,9 @@ def test_program_cache_eviction_frees_page_locked_tables(tmp_path):
 
 def test_two_caller_streams_with_small_and_tiled_matrices():
     """Two shards stepped at the same time on two caller streams (own workspaces), each with
-    small matrices (on chip, on a side stream beside the tiled products) and tiled ones:
-    every result equals that shard stepped alone on the default stream, bit for bit."""
-    shapes = [(64, 64), (96, 128), (384, 1024), (300, 520)]
+    small matrices (on chip, one CTA and a CTA pair, on a side stream beside the tiled products) and
+    tiled ones: every result equals that shard stepped alone on the default stream, bit for bit."""
+    shapes = [(64, 64), (96, 128), (384, 1024), (300, 520), (200, 240)]
     runs = {k: Run(shapes, R=1, seed=s_) for k, s_ in (("a", 71), ("b", 72), ("ra", 71), ("rb", 72))}
     runs["ra"].step()
     runs["rb"].step()
@@ -552,15 +552,56 @@ def test_small_matrices_on_chip(ns_steps):
     check_against_oracle(run, [True] * len(SMALL_SHAPES), run.p0, run.m0, ns_steps=ns_steps, tol=tols)
 
 
+PAIR_SHAPES = [(256, 256), (129, 256), (256, 129), (200, 240), (240, 200), (136, 136), (255, 256), (256, 255),
+               (129, 129)]
+
+
+@pytest.mark.parametrize("ns_steps", [1, 2, 5])
+def test_small_pair_matrices_on_chip(ns_steps):
+    """128 < m <= 256 and n <= 256: every Newton-Schulz step on a CTA pair with each CTA holding half of
+    every iterate's rows in shared memory (one ns_small_pair launch for all of them), against the fp64
+    oracle: ragged m and n on both CTAs' halves, tall and wide, the largest admitted shape, the
+    smallest m the pair takes.  The single-CTA matrices of the shard run beside them."""
+    from tests.bf16_model import orthogonalise_bf16
+    shapes = PAIR_SHAPES + [(64, 64), (96, 200)]
+    run = Run(shapes, R=1, seed=7)
+    cz.cz_profile_enable(True)
+    try:
+        run.step(ns_steps=ns_steps)
+        prof = cz.cz_profile_read()
+    finally:
+        cz.cz_profile_enable(False)
+    assert prof["ns_small"][1] == 2                 # the single-CTA launch and the CTA-pair launch
+    assert all(prof[k][1] == 0 for k in ("ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused"))
+    tols = []
+    D = run.D.cpu()
+    for i, (r, c) in enumerate(shapes):
+        _, u = OM.momentum(run.tensor(run.g, i).numpy(), np.zeros((r, c), np.float32), MU)
+        ref = OM.orthogonalise(u, ns_steps)
+        model = orthogonalise_bf16(u, ns_steps)
+        tols.append(max(UPDATE_TOL, 1.5 * rel_fro(model, ref)))
+        got = run.tensor(D, i).numpy() / (LR * OM.shape_scale(r, c))
+        assert rel_fro(got, model) <= 1e-2, ("vs rounding model", (r, c), rel_fro(got, model))
+    check_against_oracle(run, [True] * len(shapes), run.p0, run.m0, ns_steps=ns_steps, tol=tols)
+
+
 def test_small_on_chip_and_tiled_paths_are_bit_identical(tmp_path):
-    """The on-chip kernel keeps the tiled kernels' arithmetic (same K order of the
-    products, same folding, same bf16 rounding points), so sending the small
-    matrices through the tiled GEMMs instead gives the same bits; the shard mixes
-    small matrices with one the tiled path must take (m = 256)."""
-    shapes = SMALL_SHAPES + [(256, 256)]
+    """The on-chip kernels (one CTA, or a CTA pair) keep the tiled kernels' arithmetic
+    (same K order of the products, same folding, same bf16 rounding points), so
+    sending the small matrices through the tiled GEMMs instead gives the same bits;
+    the shard mixes small matrices of both kinds with one the tiled path must take
+    (m = 384), so both on-chip launches run on the side stream, one after the other."""
+    shapes = SMALL_SHAPES + PAIR_SHAPES + [(384, 512)]
     on = _run_child(tmp_path, "CZ_NS_SMALL", "1", shapes)
     off = _run_child(tmp_path, "CZ_NS_SMALL", "0", shapes)
-    assert on["launches"]["ns_small"] == 2 and off["launches"]["ns_small"] == 0
+    assert on["launches"]["ns_small"] == 4 and off["launches"]["ns_small"] == 0
+    assert torch.equal(on["M"], off["M"])
+    assert torch.equal(on["P"], off["P"])
+    # no tiled matrix: the CTA-pair launch runs on the caller's stream beside the single-CTA one
+    shapes = SMALL_SHAPES[:4] + PAIR_SHAPES[:4]
+    on = _run_child(tmp_path, "CZ_NS_SMALL", "1", shapes)
+    off = _run_child(tmp_path, "CZ_NS_SMALL", "0", shapes)
+    assert on["launches"]["ns_small"] == 4 and off["launches"]["ns_small"] == 0
     assert torch.equal(on["M"], off["M"])
     assert torch.equal(on["P"], off["P"])
 

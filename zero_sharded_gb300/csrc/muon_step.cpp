@@ -66,6 +66,7 @@ struct Group {
   int64_t off_x[2] = {0, 0}, off_a = 0, off_b = 0;   // workspace byte offsets (X ping-pong, A, B')
   bool has_wide = false, has_tall = false;
   bool small = false;          // every Newton-Schulz step on chip (ns_small), no tiled GEMMs
+  bool small_pair = false;     // ... on a CTA pair (128 < m <= 256): ns_small_pair
 };
 
 struct Layout {
@@ -75,7 +76,7 @@ struct Layout {
   int64_t off_status = 0, off_sigma = 0, off_partial = 0, off_momtiles = 0, off_mommats = 0, off_matinfo = 0;
   int64_t off_small = 0;           // SmallMat per matrix of the small groups
   int64_t off_tiledone = 0;        // momentum pass: per-tensor tile arrival counters (int32, zero)
-  int32_t n_small = 0;
+  int32_t n_small = 0;             // single-CTA and CTA-pair small matrices (SmallMat entries)
   int64_t off_tiles = 0;           // all GEMM tile lists
   int64_t n_gemm_tiles = 0;
   int64_t off_cta = 0;             // per launch: grid+1 tile offsets (int32)
@@ -89,8 +90,9 @@ struct Layout {
   int64_t bytes = 0;
 };
 
-// Small groups (m <= 128, n <= 256) take the on-chip kernel (default);
-// CZ_NS_SMALL=0 sends them through the tiled GEMMs like every other group.
+// Small groups (m <= 128, n <= 256: one CTA; 128 < m <= 256, n <= 256: a CTA pair)
+// take the on-chip kernels (default); CZ_NS_SMALL=0 sends them through the tiled
+// GEMMs like every other group.
 bool use_small() {
   static const bool small = [] {
     const char* e = std::getenv("CZ_NS_SMALL");
@@ -147,7 +149,8 @@ int build_layout(const Plan* p, int32_t rank, const int64_t* offsets, const int6
       G.has_wide |= !om.tall;
       L.mats.push_back(om);
     }
-    G.small = use_small() && G.m <= kSmallMaxM && G.n <= kSmallMaxN;
+    G.small = use_small() && G.m <= kSmallPairMaxM && G.n <= kSmallMaxN;
+    G.small_pair = G.small && G.m > kSmallMaxM;
     if (G.small) L.n_small += G.count;
     base += G.count;
   }
@@ -342,14 +345,17 @@ struct Program {
   // Used inside a stream capture: a CUDA graph may replay the copy out of the
   // page-locked image at any later time, so the image is never freed.
   bool captured = false;
-  // The small-matrix launch runs on a side stream, beside the tiled products,
-  // when both fit on the GPU at once (forked after the momentum pass, joined
+  // The small-matrix launches run on a side stream, beside the tiled products
+  // (or the single-CTA one beside the CTA-pair one when no tiled product is left),
+  // when both sides fit on the GPU at once (forked after the momentum pass, joined
   // before the call's work ends); events of this program.
   bool fork_small = false;
+  bool tiled = false;           // some matrices take the tiled products
   cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   MomParams mom{};
   std::vector<Launch> gram[2], poly, update[2], apply[2];   // [cur]: X buffer read
-  SmallParams small{};
+  SmallParams small{};          // single-CTA matrices (m <= 128)
+  SmallParams small_pair{};     // CTA-pair matrices (128 < m <= 256), SmallMat entries after the single ones
 
   Program() = default;
   Program(const Program&) = delete;
@@ -656,9 +662,10 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   const int max_grid = gemm_max_units(pair);
   std::vector<ProbDesc> gram[2], poly, upd[2], app[2];
   SmallMat* smt = at<SmallMat>(img, tb, L.off_small);
-  int32_t n_small = 0;
-  for (const Group& G : L.groups) {
-    if (G.small) {
+  int32_t n_small = 0, n_small_single = 0;
+  for (int pass = 0; pass < 2; ++pass) {        // the single-CTA matrices first, then the CTA-pair ones
+    for (const Group& G : L.groups) {
+      if (!G.small || G.small_pair != (pass == 1)) continue;
       for (int j = 0; j < G.count; ++j) {
         SmallMat& e = smt[n_small++];
         e.x = reinterpret_cast<const uint16_t*>(ws + G.off_x[0]) + (int64_t)j * G.m * G.ldx;
@@ -669,8 +676,11 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
         e.mat = G.mat_base + j;
         e.pad = 0;
       }
-      continue;
     }
+    if (pass == 0) n_small_single = n_small;
+  }
+  for (const Group& G : L.groups) {
+    if (G.small) continue;
     uint16_t* X[2] = {reinterpret_cast<uint16_t*>(ws + G.off_x[0]), reinterpret_cast<uint16_t*>(ws + G.off_x[1])};
     uint16_t* A = reinterpret_cast<uint16_t*>(ws + G.off_a);
     uint16_t* B = reinterpret_cast<uint16_t*>(ws + G.off_b);
@@ -783,7 +793,7 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   }
   SmallParams& sp = P.small;
   sp.mats = reinterpret_cast<const SmallMat*>(ws + L.off_small);
-  sp.n_mats = n_small;
+  sp.n_mats = n_small_single;
   sp.ns_steps = 0;                // set per call
   sp.sigma = mp.sigma;
   sp.info = common.mats;
@@ -796,6 +806,9 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
   sp.dbg = o.debug_update_out;
   sp.status = mp.status;
   sp.timeout_ns = kDefaultTimeoutNs;
+  P.small_pair = sp;
+  P.small_pair.mats = sp.mats + n_small_single;
+  P.small_pair.n_mats = n_small - n_small_single;
   // cannot happen: both regions are sized by build_layout
   if (cursor > L.n_gemm_tiles || cta_cursor > L.n_cta_entries) return CZ_ERR_NOMEM;
 
@@ -890,14 +903,22 @@ int build_program(const Plan* plan, int32_t rank, float* flat_param, const void*
       }
     }
   }
-  // The small-matrix CTAs beside the tiled products' units: only when all of them
-  // fit on the GPU at once (then neither waits for the other's SMs).
+  // The small-matrix CTAs beside the other side's work: beside the tiled products'
+  // units (the side stream runs the single-CTA launch, then the CTA-pair one) or,
+  // with no tiled product, the single-CTA launch beside the CTA-pair one; only when
+  // both sides fit on the GPU at once (then neither waits for the other's SMs).
   bool tiled = false;
   for (const Group& G : L.groups) tiled |= !G.small;
+  P.tiled = tiled;
+  const int64_t pair_ctas = 2 * (int64_t)(n_small - n_small_single);
+  int64_t need = -1;
+  if (tiled && n_small > 0)
+    need = (int64_t)units * (pair ? 2 : 1) + std::max<int64_t>(n_small_single, pair_ctas);
+  else if (!tiled && n_small_single > 0 && pair_ctas > 0)
+    need = n_small_single + pair_ctas;
   int dev = 0, sms = 0;
-  if (n_small > 0 && tiled && cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-      (int64_t)units * (pair ? 2 : 1) + n_small <= sms) {
+  if (need >= 0 && cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && need <= sms) {
     if (cudaEventCreateWithFlags(&P.fork_ev, cudaEventDisableTiming) == cudaSuccess &&
         cudaEventCreateWithFlags(&P.join_ev, cudaEventDisableTiming) == cudaSuccess)
       P.fork_small = true;
@@ -1114,20 +1135,32 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
       if (ev) cudaStreamWaitEvent(s, ev, 0);
     }
   } join;
-  if (P.small.n_mats > 0) {
-    SmallParams sp = P.small;
-    sp.ns_steps = ns_steps;
-    sp.a = opts->a; sp.b = opts->b; sp.c = opts->c; sp.lr = lr; sp.lr_dev = opts->lr_device;
+  if (P.small.n_mats > 0 || P.small_pair.n_mats > 0) {
+    SmallParams sp = P.small, spp = P.small_pair;
+    for (SmallParams* x : {&sp, &spp}) {
+      x->ns_steps = ns_steps;
+      x->a = opts->a; x->b = opts->b; x->c = opts->c; x->lr = lr; x->lr_dev = opts->lr_device;
+    }
+    auto single = [&](cudaStream_t st) {
+      return sp.n_mats > 0 ? traced(7, st, [&] { return launch_ns_small(sp, st); }) : cudaSuccess;
+    };
+    auto pairs = [&](cudaStream_t st) {
+      return spp.n_mats > 0 ? traced(7, st, [&] { return launch_ns_small_pair(spp, st); }) : cudaSuccess;
+    };
     cudaStream_t side = (P.fork_small && !capturing) ? side_stream(s) : nullptr;
     if (side) {
+      // side: the single-CTA launch, and the CTA-pair one too when tiled products
+      // take s; otherwise the CTA-pair launch runs on s beside it
       if (cudaEventRecord(P.fork_ev, s) != cudaSuccess || cudaStreamWaitEvent(side, P.fork_ev, 0) != cudaSuccess)
         return CZ_ERR_CUDA;
-      const cudaError_t e = traced(7, side, [&] { return launch_ns_small(sp, side); });
+      cudaError_t e = single(side);
+      if (e == cudaSuccess && P.tiled) e = pairs(side);
       if (cudaEventRecord(P.join_ev, side) != cudaSuccess) return CZ_ERR_CUDA;
       join.s = s;
       join.ev = P.join_ev;
       if (e != cudaSuccess) return CZ_ERR_CUDA;
-    } else if (traced(7, s, [&] { return launch_ns_small(sp, s); }) != cudaSuccess) {
+      if (!P.tiled && pairs(s) != cudaSuccess) return CZ_ERR_CUDA;
+    } else if (single(s) != cudaSuccess || pairs(s) != cudaSuccess) {
       return CZ_ERR_CUDA;
     }
   }

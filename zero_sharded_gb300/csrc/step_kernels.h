@@ -189,9 +189,12 @@ int gemm_max_units(bool pair);   // units that can be resident at once (persiste
 // ------------------------------------------------------------------ small-matrix Newton-Schulz
 // Matrices with m <= kSmallMaxM and n <= kSmallMaxN run every Newton-Schulz step
 // in one CTA with X, A and B' resident in shared memory and the accumulators
-// in TMEM (one CTA per matrix, one launch for all of them).
+// in TMEM (one CTA per matrix, one launch for all of them).  Matrices with
+// kSmallMaxM < m <= kSmallPairMaxM and n <= kSmallMaxN do the same on a CTA pair
+// (one cluster of two CTAs per matrix, half of every iterate's rows each).
 constexpr int kSmallMaxM = 128;
 constexpr int kSmallMaxN = 256;
+constexpr int kSmallPairMaxM = 256;
 
 struct SmallMat {
   const uint16_t* x;      // bf16 X (m x n), row pitch ldx (written by the momentum pass)
@@ -219,5 +222,6 @@ struct SmallParams {
 };
 
 cudaError_t launch_ns_small(const SmallParams& p, cudaStream_t s);
+cudaError_t launch_ns_small_pair(const SmallParams& p, cudaStream_t s);   // p.mats: CTA-pair matrices
 
 }  // namespace cz
