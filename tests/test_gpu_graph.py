@@ -129,8 +129,9 @@ def test_step_replayed_from_a_cuda_graph(tmp_path, fused):
     eager steps bit for bit (fp32 master, momentum, bf16 copy), with the fused launch and
     with one launch per product; a capture that reads lr from device memory follows a
     schedule written there before each replay, bit for bit as eager calls with those lr;
-    capturing builds nothing; a first call for new buffers is refused inside a capture."""
-    shapes = [(64, 64), (96, 128), (384, 1024), (1024, 384), (300, 520)]
+    capturing builds nothing; a first call for new buffers is refused inside a capture.  The
+    shard mixes tiled matrices with on-chip ones of both kinds (one CTA, a CTA pair)."""
+    shapes = [(64, 64), (96, 128), (384, 1024), (1024, 384), (300, 520), (200, 240)]
     f = tmp_path / f"graph_{fused}.json"
     env = dict(os.environ, CZ_NS_FUSED=fused)
     r = subprocess.run([sys.executable, "-c", _CHILD, str(f), json.dumps(shapes)], env=env,
