@@ -178,7 +178,7 @@ def load_peaks():
 
 # ------------------------------------------------------------------ workloads
 WORKLOADS = ["qwen3-32b-shard", "qwen3-1.7b-layer", "tiny", "qwen3-1.7b-28L", "qwen3-14b-microgroup",
-             "qwen3-32b-shard-flops", "qwen3-32b-shard-numel-maxflops", "qwen3-32b-ffn-pair"]
+             "qwen3-32b-shard-flops", "qwen3-32b-shard-numel-maxflops", "qwen3-32b-ffn-pair", "qwen3-14b-ffn-pair"]
 DEFAULT_WORKLOAD = "qwen3-32b-shard"
 QWEN32_LAYOUT = "qwen3-32b 64 layers in reverse layer order, 448 tensors, 320 buckets of >= 40M elements"
 
@@ -249,6 +249,12 @@ def build_workload(name: str, world: int, rank: int, planner="cz"):
         # one up (25600 x 5120, tall) and one down (5120 x 25600, wide) matrix of the Qwen3-32B shard: the
         # headline shard's kernels at its shapes on a few GB of device memory (profiling captures)
         w = wl.Workload("qwen3-32b-ffn-pair", [(25600, 5120), (5120, 25600)], ["up", "down"], 0.02, 1e-3)
+        return w, [2], 1, 1.0, 0, {"R": 1, "alpha": 1.0}
+    if name == "qwen3-14b-ffn-pair":
+        # one gate/up (17408 x 5120, tall) and one down (5120 x 17408, wide) matrix of the Qwen3-14B shapes, bf16
+        # gradients as in the micro-group: its FFN kernels at their shapes on a few GB (profiling captures)
+        w = wl.Workload("qwen3-14b-ffn-pair", [(17408, 5120), (5120, 17408)], ["up", "down"], 0.02, 1e-3,
+                        grad_bf16=True)
         return w, [2], 1, 1.0, 0, {"R": 1, "alpha": 1.0}
     if name == "qwen3-1.7b-28L":
         w = wl.qwen3_1p7b_layers(28)
