@@ -585,6 +585,29 @@ def test_small_pair_matrices_on_chip(ns_steps):
     check_against_oracle(run, [True] * len(shapes), run.p0, run.m0, ns_steps=ns_steps, tol=tols)
 
 
+def test_more_small_matrices_than_the_gpu_holds_at_once():
+    """90 CTA-pair matrices (180 CTAs of 193 KB shared memory, one per SM: more than the GPU's SMs, so the
+    clusters run in waves) and 170 single-CTA ones in one shard: both on-chip launches cannot be resident
+    together, so they run one after the other on the caller's stream; every tensor against the fp64
+    oracle."""
+    from tests.bf16_model import orthogonalise_bf16
+    shapes = [(200, 240)] * 45 + [(240, 200)] * 45 + [(64, 96)] * 85 + [(96, 64)] * 85
+    run = Run(shapes, R=1, seed=9)
+    cz.cz_profile_enable(True)
+    try:
+        run.step()
+        prof = cz.cz_profile_read()
+    finally:
+        cz.cz_profile_enable(False)
+    assert prof["ns_small"][1] == 2
+    assert all(prof[k][1] == 0 for k in ("ns_gram", "ns_poly", "ns_update", "ns_update_apply", "ns_fused"))
+    tols = []
+    for i, (r, c) in enumerate(shapes):
+        _, u = OM.momentum(run.tensor(run.g, i).numpy(), np.zeros((r, c), np.float32), MU)
+        tols.append(max(UPDATE_TOL, 1.5 * rel_fro(orthogonalise_bf16(u, 5), OM.orthogonalise(u, 5))))
+    check_against_oracle(run, [True] * len(shapes), run.p0, run.m0, tol=tols)
+
+
 def test_small_on_chip_and_tiled_paths_are_bit_identical(tmp_path):
     """The on-chip kernels (one CTA, or a CTA pair) keep the tiled kernels' arithmetic
     (same K order of the products, same folding, same bf16 rounding points), so
