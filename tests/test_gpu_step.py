@@ -272,10 +272,11 @@ def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
 
 @pytest.mark.parametrize("ns_steps", [5, 2])
 def test_paced_per_product_launches_are_bit_identical(tmp_path, ns_steps):
-    """One launch per product, each wave of tiles started together (a launch whose tiles all cost the
-    same) or not (CZ_NS_PACE=0): the same tiles on the same units in the same order, so the same bits.
-    The shapes mix K values, so some launches are paced and some are not."""
-    shapes = [(384, 1024), (1024, 384), (256, 256), (128, 640), (640, 640), (768, 768)]
+    """One launch per product, waves of tiles started together or not (CZ_NS_PACE=0): the same tiles on
+    the same units in the same order, so the same bits.  The Gram launch holds 120 tiles of two K values
+    (5120 and 4096, 80 and 64 k-blocks): more than the GPU has units, so its second wave waits for the
+    first (the paced prefix every unit has); the Poly and Update tiles (K = 1024) are not paced."""
+    shapes = [(1024, 4096)] * 4 + [(4096, 1024)] * 4 + [(1024, 5120)] * 2 + [(5120, 1024)] * 2
     paced = _run_child(tmp_path, "CZ_NS_PACE", "1", shapes, ns_steps=ns_steps, extra_env={"CZ_NS_FUSED": "0"})
     plain = _run_child(tmp_path, "CZ_NS_PACE", "0", shapes, ns_steps=ns_steps, extra_env={"CZ_NS_FUSED": "0"})
     assert paced["launches"]["ns_fused"] == 0 and paced["launches"]["ns_gram"] == 2 * ns_steps

@@ -250,14 +250,17 @@ bool use_fused() {
   return fused;
 }
 
-// One-product launches of equal-cost tiles start each wave of tiles together
-// (default): tiles that share an operand then read it at the same k, while it is
-// in the L2.  On the Qwen3-32B shard Gram's DRAM reads fell 27% per matrix and its
-// time 1.5-1.7%; the step went from 53.40 to 52.98 ms on one box and did not move
-// on another.  Without it the units drift apart over a launch of ~210 tiles each,
-// and a launch over 8 matrices read per matrix about twice what one over 2 read.
-// Letting units run up to 1, 2 or 4 waves apart did not help.  CZ_NS_PACE=0 turns
-// it off.
+// One-product launches start each wave of tiles together (default): tiles that
+// share an operand then read it at the same k, while it is in the L2.  On the
+// Qwen3-32B shard Gram's DRAM reads fell 27% per matrix; the step went from 53.40 to
+// 52.98 ms on one box, from 54.57 to 53.85 on another, and did not move on a third.
+// A launch whose tiles differ in K is paced over the waves every unit has (its
+// heaviest K): the Qwen3-14B micro-group went from 173.3 to 170.2 ms.  Tiles of
+// fewer than kPaceMinKBlocks k-blocks are not paced: waiting for the slowest unit at
+// every short tile cost more than it saved (the Qwen3-1.7B x 28 set's Poly, 32
+// k-blocks, went from 4.81 to 5.00 ms per step).  Letting units run up to 1, 2 or 4
+// waves apart did not help.  CZ_NS_PACE=0 turns it off.
+constexpr int64_t kPaceMinKBlocks = 64;
 bool use_pace() {
   static const bool on = [] {
     const char* e = std::getenv("CZ_NS_PACE");
@@ -319,7 +322,7 @@ struct Launch {
   int phase;
   int first;
   int cur;                          // X buffer read (Gram, Update, Apply)
-  bool uniform = false;             // every tile has the same k-blocks (wave pacing applies)
+  int32_t pace_tiles = 0;           // wave pacing of each unit's first pace_tiles tiles (0: none)
   GemmParams params;
 };
 
@@ -535,8 +538,15 @@ bool make_launches(int phase, std::vector<ProbDesc>& probs, int4* dev_tiles, int
     ln.phase = phase;
     ln.first = first;
     ln.cur = cur;
-    ln.uniform = true;
-    for (size_t i = c0 + 1; i < c1; ++i) ln.uniform = ln.uniform && probs[i].gp.K == probs[c0].gp.K;
+    // Wave pacing covers the tiles every unit has: the shortest list's length, plus
+    // the next tile (it waits only for tiles every unit issues).  LPT deals the
+    // heaviest tiles first, round-robin, so those waves hold tiles of one K.  Only
+    // launches whose heaviest tiles have at least kPaceMinKBlocks k-blocks are paced.
+    {
+      size_t mn = per[0].size();
+      for (int b = 1; b < grid; ++b) mn = std::min(mn, per[b].size());
+      ln.pace_tiles = (tl.front().cost - 2 >= kPaceMinKBlocks && mn >= 1) ? (int32_t)mn + 1 : 0;
+    }
     std::memset(&ln.params, 0, sizeof(GemmParams));
     ln.params = common;
     ln.params.n_prob = (int)(c1 - c0);
@@ -1202,7 +1212,8 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
     gp = ln.params;
     gp.first = first;
     scalars(gp);
-    gp.pace = (use_pace() && ln.uniform) ? pace_base + (size_t)(t * 3 + slot) * pace_stride : nullptr;
+    gp.pace = (use_pace() && ln.pace_tiles >= 2) ? pace_base + (size_t)(t * 3 + slot) * pace_stride : nullptr;
+    gp.pace_tiles = ln.pace_tiles;
     cudaError_t e = traced(kind, s, [&] { return launch_ns_gemm(phase, P.pair, gp, s); });
     if (e != cudaSuccess && gp.pace && refused(e)) {
       cudaGetLastError();

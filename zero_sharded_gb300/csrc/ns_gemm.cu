@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(threads_of(PHASE), 1) ns_gemm_kernel(const __g
         if constexpr (!is_fused(PHASE)) {
           // wave pacing: this tile starts once every unit has issued as many tiles as this
           // one (the even CTA paces; the odd one follows through the shared stage ring)
-          if (p.pace && rank == 0 && issued_tiles > 0 &&
+          if (p.pace && rank == 0 && issued_tiles > 0 && issued_tiles < p.pace_tiles &&
               !counter_wait(p.pace, issued_tiles * p.grid, abort, p.status, p.timeout_ns))
             break;
         }

@@ -143,11 +143,14 @@ struct GemmParams {
   float* dbg;             // debug delta or null (kApply)
   int* status;
   int64_t timeout_ns;
-  // one-product launches of equal-cost tiles: null, or a counter of the tiles whose
-  // operand loads the units have issued.  A unit starts its j-th tile once every unit
+  // one-product launches: null, or a counter of the tiles whose operand loads the
+  // units have issued.  A unit starts its j-th tile, j < pace_tiles, once every unit
   // has issued j tiles (j * grid), so each wave of tiles starts together and the
-  // tiles sharing an operand read it at the same k (cooperative launch)
+  // tiles sharing an operand read it at the same k (cooperative launch).  Every unit
+  // has at least pace_tiles - 1 tiles, so the least advanced unit never waits.
   int* pace;
+  int32_t pace_tiles;
+  int32_t pad_pace;
   // fused launch (kFused) only
   int32_t ns_steps;
   int32_t n_mats;
