@@ -133,13 +133,13 @@ KIND_SOURCE = {"ns_fused": "ns_gemm", "ns_gram": "ns_gemm", "ns_poly": "ns_gemm"
                "ns_update_apply": "ns_gemm", "momentum": "momentum", "ns_small": "ns_small", "apply": "apply"}
 NCU_TRAFFIC = {
     # kernel source group: (source hash, {workload: {kind: bytes per launch}})
-    "ns_gemm": ("286ad3fc03d29170", {"qwen3-1.7b-layer": {"ns_fused": 2623.08e6},
-                                     "qwen3-32b-R32-shard4": {"ns_gram": 5903.29e6, "ns_poly": 959.19e6,
-                                                              "ns_update": 11151.57e6, "ns_update_apply": 24229.18e6}}),
-    "momentum": ("367f4515ac681fd5", {"qwen3-1.7b-layer": {"momentum": 648.56e6},
-                                      "qwen3-32b-R32-shard4": {"momentum": 14626.38e6}}),
-    # the tiny workload's two on-chip launches per step (one CTA: 0.343 MB, CTA pair: 0.449 MB), averaged
-    "ns_small": ("b0873ff2dc8d9e5a", {"tiny": {"ns_small": 0.3954e6}}),
+    "ns_gemm": ("ed6e332a2132d77b", {"qwen3-1.7b-layer": {"ns_fused": 2609.48e6},
+                                     "qwen3-32b-R32-shard4": {"ns_gram": 5905.45e6, "ns_poly": 993.78e6,
+                                                              "ns_update": 11097.07e6, "ns_update_apply": 24284.40e6}}),
+    "momentum": ("abb7cc086cbae0af", {"qwen3-1.7b-layer": {"momentum": 648.84e6},
+                                      "qwen3-32b-R32-shard4": {"momentum": 14626.10e6}}),
+    # the tiny workload's two on-chip launches per step (one CTA: 0.342 MB, CTA pair: 0.448 MB), averaged
+    "ns_small": ("b100f296afbd2642", {"tiny": {"ns_small": 0.3950e6}}),
     "apply": ("a6d9356fa7fabfff", {"qwen3-1.7b-layer": {"apply": 649.76e6}}),
 }
 

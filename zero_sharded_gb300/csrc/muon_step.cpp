@@ -1199,13 +1199,13 @@ int muon_step(const cz_plan* plan, int32_t rank, float* flat_param, const void* 
       return CZ_ERR_CUDA;
     cudaGetLastError();
   }
-  // One launch of a product.  A launch whose tiles all cost the same (round-robin
-  // lists: the units' list lengths differ by at most one) is paced by a counter of
-  // its own, one per (step, product) in the fused launch's completion counters
-  // (zeroed by every call's table copy; the fused launch does not run in a call
-  // that takes this path).  The least advanced unit never waits, so the pacing
-  // cannot deadlock once every unit is resident, which the cooperative attribute
-  // guarantees; a refused cooperative launch runs again unpaced.
+  // One launch of a product.  A launch with pace_tiles >= 2 (make_launches: the
+  // waves every unit has, heaviest tiles of at least kPaceMinKBlocks k-blocks) is
+  // paced by a counter of its own, one per (step, product) in the fused launch's
+  // completion counters (zeroed by every call's table copy; the fused launch does not
+  // run in a call that takes this path).  The least advanced unit never waits, so the
+  // pacing cannot deadlock once every unit is resident, which the cooperative
+  // attribute guarantees; a refused cooperative launch runs again unpaced.
   int* pace_base = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + P.L.off_done);
   const size_t pace_stride = (size_t)std::max<size_t>(P.L.mats.size(), 1);
   auto run = [&](const Launch& ln, int phase, int kind, int first, int t, int slot) -> cudaError_t {
