@@ -270,6 +270,23 @@ def test_fused_and_per_product_launches_are_bit_identical(tmp_path):
     assert torch.equal(on["P"], plain["P"])
 
 
+@pytest.mark.parametrize("fused", ["1", "0"])
+def test_single_cta_tiles_and_cta_pair_tiles_are_bit_identical(tmp_path, fused):
+    """CZ_NS_PAIR=0: the tiled products on single CTAs (128 x 256 tiles, cta_group::1) instead of CTA pairs
+    (256 x 256, cta_group::2), in the fused launch and in one launch per product.  Each output element is
+    accumulated over the same K sequence and rounded at the same points, so the bits agree; the shard also
+    holds on-chip matrices of both kinds (their kernels do not depend on the switch)."""
+    shapes = [(384, 1024), (1024, 384), (640, 640), (300, 520), (64, 96), (200, 240)]
+    single = _run_child(tmp_path, "CZ_NS_PAIR", "0", shapes, extra_env={"CZ_NS_FUSED": fused})
+    pair = _run_child(tmp_path, "CZ_NS_PAIR", "1", shapes, extra_env={"CZ_NS_FUSED": fused})
+    if fused == "1":
+        assert single["launches"]["ns_fused"] == 2 and pair["launches"]["ns_fused"] == 2
+    else:
+        assert single["launches"]["ns_gram"] >= 10 and pair["launches"]["ns_gram"] >= 10
+    assert torch.equal(single["M"], pair["M"])
+    assert torch.equal(single["P"], pair["P"])
+
+
 @pytest.mark.parametrize("ns_steps", [5, 2])
 def test_paced_per_product_launches_are_bit_identical(tmp_path, ns_steps):
     """One launch per product, waves of tiles started together or not (CZ_NS_PACE=0): the same tiles on
